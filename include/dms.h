@@ -1,0 +1,137 @@
+/*
+ * dms.h -- C ABI of the DMS decode-attention library (libdms.so).
+ *
+ * Dynamic Memory Sparsification (DMS) keeps, for every (sequence, KV head), a
+ * compacted KV cache: each appended token carries a binary eviction decision,
+ * and a token marked for eviction leaves the cache w steps after it was
+ * appended ("Inference-Time Hyper-Scaling with KV Cache Compression", AI
+ * research-map summary, section "Approach": a learned per-head binary eviction
+ * decision whose eviction is executed after a delay window; the window is 16
+ * tokens in that summary's "Measured effects reported in the paper" table).
+ * Decoding is bound by reading the KV cache from memory (same paper, notes
+ * page, section "研究背景与动机": every autoregressive step reads the whole
+ * cache), so the library streams only the retained K/V bytes.
+ *
+ * Conventions for every call:
+ *  - Tensor arguments are DEVICE pointers on the cache's device, caller-owned,
+ *    contiguous, row-major, 16-byte aligned.  They are read or written in
+ *    stream order and are not retained after the enqueued work completes.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All work of a
+ *    cache must be enqueued on one stream; a cache is not thread-safe.
+ *  - Return value: DMS_OK (0) or a negative DMS_ERR_* code.  Argument errors
+ *    are detected on the host and enqueue nothing.  Errors raised on the
+ *    device (capacity overflow, a timed-out wait) are sticky and surface at
+ *    dms_cache_status().
+ *  - bf16 means IEEE-754 binary16-brain (__nv_bfloat16), passed as void*.
+ */
+#ifndef DMS_H
+#define DMS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DMS_OK 0
+#define DMS_ERR_INVALID_ARG (-1) /* bad size, null or misaligned pointer, wrong device */
+#define DMS_ERR_CUDA (-2)        /* a CUDA allocation, copy or launch failed */
+#define DMS_ERR_CAPACITY (-3)    /* sticky: an append found no free slot */
+#define DMS_ERR_BAD_HANDLE (-4)  /* NULL, destroyed or foreign cache handle */
+#define DMS_ERR_TIMEOUT (-5)     /* sticky: a device-side wait passed its time limit */
+#define DMS_ERR_EMPTY (-6)       /* decode before any token was appended */
+
+/* Largest query-head group per KV head (Hq / Hkv) the decode kernel supports. */
+#define DMS_MAX_GROUP 8
+
+typedef struct dms_cache dms_cache_t;
+
+/*
+ * Create a cache for `batch` sequences x `kv_heads` KV heads, each with
+ * `capacity` slots of `head_dim` bf16 elements for K and for V, and delay
+ * window `window` (>= 1; 16 in the method).  head_dim must be 64 or 128.
+ * Allocates on the current CUDA device: K and V pools bf16
+ * [batch][kv_heads][capacity][head_dim], the slot -> position map int32
+ * [batch][kv_heads][capacity], the ring of the last `window` appends
+ * (slot, decision), the lengths int32 [batch][kv_heads], a sticky error word
+ * and the split-K scratch of the decode kernel; all zeroed.  The host keeps the
+ * position counter t (all sequences advance in lock step).
+ * Returns NULL on failure; dms_last_error() then gives the code.
+ */
+dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_dim, int window);
+
+/* Code of the last failed dms_cache_create() on this thread (DMS_OK if none). */
+int dms_last_error(void);
+
+/* Free the cache's device memory.  Synchronizes the device first.  NULL or an
+ * unknown handle is ignored. */
+void dms_cache_destroy(dms_cache_t* cache);
+
+/*
+ * Append token t (= the number of tokens appended so far) to every
+ * (sequence, KV head) -- the method's decision, delayed eviction and slot reuse
+ * in one kernel, with no host round trip:
+ *   k, v         bf16  [batch][kv_heads][head_dim]   the new token's K and V
+ *   evict_logit  fp32  [batch][kv_heads]             decision = (logit > 0)
+ * Per (b, h): if t >= window and token t - window was marked, that token leaves
+ * and token t takes its slot; otherwise token t takes slot len and len grows.
+ * With no free slot the token is dropped and DMS_ERR_CAPACITY is latched.
+ * The host counter t advances by one.
+ */
+int dms_append(dms_cache_t* cache, const void* k, const void* v, const float* evict_logit,
+               void* stream);
+
+/*
+ * Append `chunk` tokens (positions t .. t+chunk-1) in one launch; the result
+ * is bit-identical to `chunk` calls of dms_append:
+ *   k, v    bf16 [batch][kv_heads][chunk][head_dim]
+ *   logits  fp32 [batch][kv_heads][chunk]
+ * Used to fill the cache before decoding (the bookkeeping half of a chunked
+ * prefill).
+ */
+int dms_append_chunk(dms_cache_t* cache, const void* k, const void* v, const float* logits,
+                     int chunk, void* stream);
+
+/*
+ * Decode attention for the query of the last appended token, over every
+ * retained slot of each (sequence, KV head):
+ *   q    bf16 [batch][q_heads][head_dim]
+ *   out  fp32 [batch][q_heads][head_dim]
+ *   out[b][g] = softmax(scale * K_h q_g) V_h over the retained keys of KV head
+ *   h = g / (q_heads / kv_heads), in fp32 (bf16 inputs widened exactly).
+ * q_heads must be a multiple of kv_heads with q_heads / kv_heads <= 8.
+ * The retained slots of all heads are split evenly across the warps of a
+ * persistent grid (flash-decoding split-K balanced by retained length); the
+ * partial results of a head split across warps are merged on the device by
+ * the last warp to finish it.  Returns DMS_ERR_EMPTY if nothing was appended.
+ */
+int dms_decode_attention(dms_cache_t* cache, const void* q, float* out, float scale, int q_heads,
+                         void* stream);
+
+/* Copy the retained length of every (sequence, KV head) into out_dev
+ * (int32 [batch][kv_heads], device memory), stream-ordered. */
+int dms_cache_lengths(dms_cache_t* cache, int32_t* out_dev, void* stream);
+
+/* Copy the slot -> position map into out_dev (int32 [batch][kv_heads][capacity];
+ * -1 = slot never written).  Slots [0, len) hold exactly the retained tokens. */
+int dms_cache_slot_positions(dms_cache_t* cache, int32_t* out_dev, void* stream);
+
+/* Copy the K and V pools, in logical element order, into k_out / v_out
+ * (bf16 [batch][kv_heads][capacity][head_dim] each, device memory). */
+int dms_cache_export_kv(dms_cache_t* cache, void* k_out, void* v_out, void* stream);
+
+/* Synchronize `stream`, then return the sticky device error (DMS_OK,
+ * DMS_ERR_CAPACITY or DMS_ERR_TIMEOUT) or DMS_ERR_CUDA if the stream failed. */
+int dms_cache_status(dms_cache_t* cache, void* stream);
+
+/* Number of tokens appended so far (the host position counter t), or -1. */
+int64_t dms_cache_position(dms_cache_t* cache);
+
+/* Static description of a code. */
+const char* dms_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DMS_H */

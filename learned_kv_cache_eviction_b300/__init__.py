@@ -1,0 +1,18 @@
+"""DMS (Dynamic Memory Sparsification) decode attention for NVIDIA B300.
+
+The compute lives in libdms.so (CUDA, sm_103a; C ABI in include/dms.h);
+``dms`` is its Python binding and ``workload`` draws seeded synthetic inputs.
+"""
+from .dms import (  # noqa: F401
+    DmsCache,
+    DmsError,
+    dms_append,
+    dms_append_chunk,
+    dms_cache_create,
+    dms_cache_destroy,
+    dms_cache_lengths,
+    dms_cache_slot_positions,
+    dms_cache_status,
+    dms_decode_attention,
+    load_library,
+)

@@ -1,0 +1,467 @@
+// decode.cuh -- split-K GQA decode attention over the DMS compacted caches.
+//
+// What it computes: for every sequence b and query head g, softmax attention
+// of q[b][g] over the retained keys of KV head h = g / G (G = Hq / Hkv).  The
+// retained keys of (b, h) are exactly slots [0, len) of its pool (the slot
+// policy in append.cuh keeps them dense), so the kernel reads only the
+// retained K/V bytes -- the cost the method is built to cut (notes page of
+// "Inference-Time Hyper-Scaling with KV Cache Compression", section
+// "研究背景与动机": each decode step reads the whole KV cache; the AI
+// research-map summary, "Experimental setup", counts "KV-cache token reads").
+//
+// Work split ("balanced by retained length"): the concatenation of all heads'
+// retained slots, S = sum(len) slots, is cut into Pe equal contiguous ranges,
+// one per warp of a persistent grid (one CTA per SM).  Each warp is an
+// independent flash-decoding worker:
+//   * lane 0 streams its range in tiles of TK slots (K tile and V tile, each
+//     one contiguous bulk copy global -> shared, completing on an mbarrier),
+//     NST tiles in flight;
+//   * QK: lane r computes the G scores of slot r of the tile over the full
+//     head dim (K rows are chunk-permuted in the pool, so these reads are free
+//     of bank conflicts while q is read as a broadcast);
+//   * online softmax in fp32, base-2 (q is pre-scaled by scale * log2 e);
+//   * PV: lane owns D/32 output elements of all G heads.
+// A head covered by one warp is written directly.  A head split across
+// warps leaves one partial (max, sum, unnormalised acc) per warp; the warp
+// that finishes such a head last (an atomic arrival counter per head, no
+// waiting) merges the partials and resets the counter.
+#pragma once
+
+#include "dms_device.cuh"
+
+namespace dms {
+
+template <int D_, int G_>
+struct DecodeShape {
+  static constexpr int D = D_;
+  static constexpr int G = G_;
+  static constexpr int NW = 4;    // warps per CTA (one CTA per SM)
+  static constexpr int TK = 32;   // slots per tile
+  static constexpr int NST = 3;   // tiles in flight per warp
+  static constexpr int CH = D / 8;
+  static constexpr int EL = D / 32;  // output elements per lane
+  static constexpr int ROWB = D * 2;
+  static constexpr int TILEB = TK * ROWB;
+  static constexpr int GP = (G + 3) / 4 * 4;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = NST * TILEB;
+  static constexpr int OFF_QRAW = 2 * NST * TILEB;
+  static constexpr int OFF_QS = OFF_QRAW + ((G * D * 2 + 127) / 128) * 128;
+  static constexpr int OFF_P = OFF_QS + G * D * 4;
+  static constexpr int OFF_BAR = OFF_P + TK * GP * 4;
+  static constexpr int WARP_BYTES = ((OFF_BAR + (NST + 1) * 8 + 127) / 128) * 128;
+  static constexpr int SMEM = NW * WARP_BYTES;
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static_assert(G >= 1 && G <= 8, "1 <= G <= 8");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+// Fewest retained slots a warp is given (bounds the number of partials when
+// the cache is small).
+constexpr int kMinSlotsPerWarp = 128;
+
+struct DecodeArgs {
+  const uint4* K;
+  const uint4* V;
+  const int32_t* len;
+  const uint16_t* q;  // bf16 [B][Hq][D]
+  float* out;         // fp32 [B][Hq][D]
+  float* part_acc;    // [entries][G][D]
+  float* part_ml;     // [entries][G][2]
+  int32_t* head_cnt;  // [NH], zero between launches
+  int32_t* err;
+  int NH, Hkv, cap;
+  float qscale;  // scale * log2(e)
+};
+
+// Retained-slot iterator over one warp's global range [A, E).
+struct TileIter {
+  int i;      // head
+  int L;      // retained length of head i
+  int s;      // next slot in head i
+  int send;   // end of this warp's slots in head i
+  int64_t P;  // global index of slot 0 of head i
+  int64_t E;
+  bool valid;
+  bool first;  // next tile opens a new segment (head)
+
+  __device__ __forceinline__ void start(const int32_t* len, int i0, int64_t P0, int64_t A, int64_t E_) {
+    i = i0;
+    P = P0;
+    E = E_;
+    L = len[i0];
+    s = static_cast<int>(A - P0);
+    send = static_cast<int>(min(E, P0 + L) - P0);
+    valid = s < send;
+    first = true;
+  }
+  __device__ __forceinline__ void advance(const int32_t* len, int NH, int cnt) {
+    s += cnt;
+    first = false;
+    if (s < send) return;
+    P += L;
+    ++i;
+    while (P < E && i < NH) {
+      L = len[i];
+      if (L > 0) break;
+      ++i;
+    }
+    if (P >= E || i >= NH) {
+      valid = false;
+      return;
+    }
+    s = 0;
+    send = static_cast<int>(min(E, P + L) - P);
+    first = true;
+  }
+};
+
+// Exclusive scan of len[0..NH) into pre[0..NH] by the whole CTA.
+__device__ __forceinline__ void scan_lengths(const int32_t* __restrict__ len, int NH, int* pre) {
+  __shared__ int wsum[32];
+  const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int per = (NH + nt - 1) / nt;
+  const int b0 = min(NH, tid * per), b1 = min(NH, b0 + per);
+  int sum = 0;
+  for (int x = b0; x < b1; ++x) sum += len[x];
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int v = lane < (nt >> 5) ? wsum[lane] : 0;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    wsum[lane] = inc - v;
+  }
+  __syncthreads();
+  int run = wsum[wid] + incl - sum;
+  for (int x = b0; x < b1; ++x) {
+    pre[x] = run;
+    run += len[x];
+  }
+  if (tid == nt - 1) pre[NH] = run;
+  __syncthreads();
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(const DecodeArgs a) {
+  using Sh = DecodeShape<D, G>;
+  constexpr int NW = Sh::NW, TK = Sh::TK, NST = Sh::NST, CH = Sh::CH, EL = Sh::EL;
+  constexpr int GP = Sh::GP, ROWB = Sh::ROWB, TILEB = Sh::TILEB;
+  extern __shared__ __align__(1024) uint8_t smem[];
+
+  // ---- prologue: prefix sums of the retained lengths, warp ranges ----
+  int* pre = reinterpret_cast<int*>(smem);  // aliases the warp regions until the barrier below
+  scan_lengths(a.len, a.NH, pre);
+  const int64_t S = pre[a.NH];
+  const int wl = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int64_t Pe = static_cast<int64_t>(gridDim.x) * NW;
+  if (S / kMinSlotsPerWarp < Pe) Pe = S / kMinSlotsPerWarp;
+  if (Pe < 1) Pe = 1;
+  const int64_t wg = static_cast<int64_t>(blockIdx.x) * NW + wl;
+  const bool active = S > 0 && wg < Pe;
+  int64_t A = 0, E = 0, P0 = 0;
+  int i0 = 0;
+  if (active) {
+    A = (wg * S) / Pe;
+    E = ((wg + 1) * S) / Pe;
+    int lo = 0, hi = a.NH;  // pre[lo] <= A < pre[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid] <= A) lo = mid; else hi = mid;
+    }
+    i0 = lo;
+    P0 = pre[lo];
+  }
+  __syncthreads();
+  if (!active) return;
+
+  // ---- per-warp shared memory ----
+  uint8_t* wbase = smem + wl * Sh::WARP_BYTES;
+  uint8_t* Ks = wbase + Sh::OFF_K;
+  uint8_t* Vs = wbase + Sh::OFF_V;
+  uint8_t* qraw = wbase + Sh::OFF_QRAW;
+  float* qs = reinterpret_cast<float*>(wbase + Sh::OFF_QS);
+  float* pb = reinterpret_cast<float*>(wbase + Sh::OFF_P);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + Sh::OFF_BAR);  // [NST] tiles, [NST] = q
+  uint64_t* qbar = bars + NST;
+  if (lane == 0) {
+    for (int x = 0; x <= NST; ++x) mbar_init(&bars[x], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  const int Hq = a.Hkv * G;
+  TileIter is, cs;
+  is.start(a.len, i0, P0, A, E);
+  cs = is;
+  int n_issued = 0, n_cons = 0, nq_issued = 0, nq_conv = 0;
+
+  // Issue tiles ahead while buffers are free.  A segment's first tile also
+  // brings that segment's q; the single q buffer must have been consumed.
+  auto try_issue = [&]() {
+    while (is.valid && n_issued < n_cons + NST) {
+      if (is.first && nq_issued != nq_conv) break;
+      const int cnt = min(TK, is.send - is.s);
+      const int buf = n_issued % NST;
+      if (lane == 0) {
+        const uint32_t bytes = static_cast<uint32_t>(cnt * ROWB);
+        const size_t row = static_cast<size_t>(is.i) * a.cap + is.s;
+        mbar_arrive_expect_tx(&bars[buf], 2 * bytes);
+        bulk_copy_g2s(Ks + buf * TILEB, a.K + row * CH, bytes, &bars[buf]);
+        bulk_copy_g2s(Vs + buf * TILEB, a.V + row * CH, bytes, &bars[buf]);
+        if (is.first) {
+          const int b = is.i / a.Hkv, h = is.i - (is.i / a.Hkv) * a.Hkv;
+          mbar_arrive_expect_tx(qbar, G * D * 2);
+          bulk_copy_g2s(qraw, a.q + (static_cast<size_t>(b) * Hq + h * G) * D, G * D * 2, qbar);
+        }
+      }
+      if (is.first) ++nq_issued;
+      ++n_issued;
+      is.advance(a.len, a.NH, cnt);
+    }
+  };
+
+  // Latch a timeout, then wait (bounded) for this warp's copies in flight.
+  auto fail_and_drain = [&]() {
+    if (lane == 0) atomicOr(a.err, kErrBitTimeout);
+    for (int k = n_cons; k < n_issued; ++k) (void)mbar_wait(&bars[k % NST], (k / NST) & 1);
+    if (nq_issued > nq_conv) (void)mbar_wait(qbar, nq_conv & 1);
+  };
+
+  float m[G], l[G];
+  float2 o[G][EL / 2];
+  int seg_i = 0, seg_L = 0;
+  int64_t seg_P = 0;
+
+  try_issue();
+  while (cs.valid) {
+    if (cs.first) {
+      // ---- segment start: this head's q (bf16) -> qs (fp32, pre-scaled) ----
+      if (nq_issued <= nq_conv || !mbar_wait(qbar, nq_conv & 1)) {
+        fail_and_drain();
+        return;
+      }
+      const uint32_t* qw = reinterpret_cast<const uint32_t*>(qraw);
+#pragma unroll
+      for (int x = lane; x < G * D / 2; x += 32) {
+        const float2 f = bf16x2_to_float2(qw[x]);
+        qs[2 * x] = f.x * a.qscale;
+        qs[2 * x + 1] = f.y * a.qscale;
+      }
+      __syncwarp();
+      ++nq_conv;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EL / 2; ++e) o[g][e] = make_float2(0.f, 0.f);
+      }
+      seg_i = cs.i;
+      seg_L = cs.L;
+      seg_P = cs.P;
+      try_issue();
+    }
+
+    const int cnt = min(TK, cs.send - cs.s);
+    const int s0 = cs.s;
+    const int buf = n_cons % NST;
+    if (n_issued <= n_cons || !mbar_wait(&bars[buf], (n_cons / NST) & 1)) {
+      fail_and_drain();
+      return;
+    }
+
+    // ---- QK: lane r scores slot s0 + r for all G heads ----
+    float sc[G];
+    {
+      const uint4* Kt = reinterpret_cast<const uint4*>(Ks + buf * TILEB);
+      if (lane < cnt) {
+        const int sw = (s0 + lane) & 7;
+        const uint4* krow = Kt + lane * CH;
+        float2 acc0[G], acc1[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          acc0[g] = make_float2(0.f, 0.f);
+          acc1[g] = make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const uint4 kk = krow[c ^ sw];
+          const float2 k0 = bf16x2_to_float2(kk.x), k1 = bf16x2_to_float2(kk.y);
+          const float2 k2 = bf16x2_to_float2(kk.z), k3 = bf16x2_to_float2(kk.w);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float4* qp = reinterpret_cast<const float4*>(qs + g * D + c * 8);
+            const float4 qa = qp[0], qb = qp[1];
+            acc0[g] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc0[g]);
+            acc1[g] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc1[g]);
+            acc0[g] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc0[g]);
+            acc1[g] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc1[g]);
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) sc[g] = (acc0[g].x + acc0[g].y) + (acc1[g].x + acc1[g].y);
+      } else {
+#pragma unroll
+        for (int g = 0; g < G; ++g) sc[g] = -INFINITY;
+      }
+    }
+
+    // ---- online softmax (base 2) ----
+    {
+      bool rescale = false;
+      float alpha[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float mt = warp_max(sc[g]);
+        const float mn = fmaxf(m[g], mt);
+        alpha[g] = fast_exp2(m[g] - mn);
+        const float p = fast_exp2(sc[g] - mn);
+        l[g] = l[g] * alpha[g] + p;
+        m[g] = mn;
+        pb[lane * GP + g] = p;
+        rescale |= alpha[g] != 1.f;
+      }
+      if (rescale) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float2 aa = make_float2(alpha[g], alpha[g]);
+#pragma unroll
+          for (int e = 0; e < EL / 2; ++e) o[g][e] = __fmul2_rn(o[g][e], aa);
+        }
+      }
+      __syncwarp();
+    }
+
+    // ---- PV: lane owns elements [lane*EL, lane*EL + EL) of every head ----
+    {
+      const uint8_t* Vt = Vs + buf * TILEB + lane * (EL * 2);
+      auto pv_row = [&](int j) {
+        float2 v2[EL / 2];
+        if constexpr (EL == 4) {
+          const uint2 vv = *reinterpret_cast<const uint2*>(Vt + j * ROWB);
+          v2[0] = bf16x2_to_float2(vv.x);
+          v2[1] = bf16x2_to_float2(vv.y);
+        } else {
+          v2[0] = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(Vt + j * ROWB));
+        }
+        float pj[GP];
+#pragma unroll
+        for (int x = 0; x < GP / 4; ++x) {
+          const float4 p4 = *reinterpret_cast<const float4*>(pb + j * GP + 4 * x);
+          pj[4 * x + 0] = p4.x;
+          pj[4 * x + 1] = p4.y;
+          pj[4 * x + 2] = p4.z;
+          pj[4 * x + 3] = p4.w;
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float2 pp = make_float2(pj[g], pj[g]);
+#pragma unroll
+          for (int e = 0; e < EL / 2; ++e) o[g][e] = __ffma2_rn(pp, v2[e], o[g][e]);
+        }
+      };
+      if (cnt == TK) {
+#pragma unroll 8
+        for (int j = 0; j < TK; ++j) pv_row(j);
+      } else {
+        for (int j = 0; j < cnt; ++j) pv_row(j);
+      }
+    }
+    __syncwarp();
+    ++n_cons;
+    const int cur_i = cs.i;
+    cs.advance(a.len, a.NH, cnt);
+    const bool seg_end = !cs.valid || cs.i != cur_i;
+
+    if (seg_end) {
+      // ---- segment end: direct output, or partial + last-arriver merge ----
+#pragma unroll
+      for (int g = 0; g < G; ++g) l[g] = warp_sum(l[g]);
+      const int b = seg_i / a.Hkv, h = seg_i - b * a.Hkv;
+      float* outp = a.out + (static_cast<size_t>(b) * Hq + h * G) * D + lane * EL;
+      const int64_t w0 = ((seg_P + 1) * Pe - 1) / S;
+      const int64_t w1 = ((seg_P + seg_L) * Pe - 1) / S;
+      if (w0 == w1) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float inv = 1.f / l[g];
+#pragma unroll
+          for (int e = 0; e < EL / 2; ++e) {
+            reinterpret_cast<float2*>(outp + g * D)[e] = make_float2(o[g][e].x * inv, o[g][e].y * inv);
+          }
+        }
+      } else {
+        const size_t idx = static_cast<size_t>(wg + seg_i);
+        float* pa = a.part_acc + idx * G * D + lane * EL;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+          for (int e = 0; e < EL / 2; ++e) reinterpret_cast<float2*>(pa + g * D)[e] = o[g][e];
+        }
+        if (lane < G) {
+          float mm = m[0], ll = l[0];
+#pragma unroll
+          for (int g = 1; g < G; ++g) {
+            if (lane == g) {
+              mm = m[g];
+              ll = l[g];
+            }
+          }
+          reinterpret_cast<float2*>(a.part_ml + idx * G * 2)[lane] = make_float2(mm, ll);
+        }
+        __threadfence();
+        __syncwarp();
+        int old = 0;
+        if (lane == 0) old = atomicAdd(&a.head_cnt[seg_i], 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == static_cast<int>(w1 - w0)) {
+          __threadfence();
+          for (int g = 0; g < G; ++g) {
+            float M = -INFINITY;
+            for (int64_t k = w0 + lane; k <= w1; k += 32) {
+              M = fmaxf(M, __ldcg(a.part_ml + (static_cast<size_t>(k + seg_i) * G + g) * 2));
+            }
+            M = warp_max(M);
+            float Ls = 0.f;
+            for (int64_t k = w0 + lane; k <= w1; k += 32) {
+              const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml) +
+                                       static_cast<size_t>(k + seg_i) * G + g);
+              Ls += ml.y * fast_exp2(ml.x - M);
+            }
+            Ls = warp_sum(Ls);
+            float2 acc[EL / 2];
+#pragma unroll
+            for (int e = 0; e < EL / 2; ++e) acc[e] = make_float2(0.f, 0.f);
+            for (int64_t k = w0; k <= w1; ++k) {
+              const size_t kk = static_cast<size_t>(k + seg_i);
+              const float wk = fast_exp2(__ldcg(a.part_ml + (kk * G + g) * 2) - M);
+              const float2* src = reinterpret_cast<const float2*>(a.part_acc + (kk * G + g) * D + lane * EL);
+#pragma unroll
+              for (int e = 0; e < EL / 2; ++e) acc[e] = __ffma2_rn(make_float2(wk, wk), __ldcg(src + e), acc[e]);
+            }
+            const float inv = 1.f / Ls;
+#pragma unroll
+            for (int e = 0; e < EL / 2; ++e) {
+              reinterpret_cast<float2*>(outp + g * D)[e] = make_float2(acc[e].x * inv, acc[e].y * inv);
+            }
+          }
+          if (lane == 0) a.head_cnt[seg_i] = 0;
+        }
+      }
+    }
+    try_issue();
+  }
+}
+
+}  // namespace dms

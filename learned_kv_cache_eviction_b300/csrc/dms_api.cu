@@ -1,0 +1,344 @@
+// dms_api.cu -- the C ABI of libdms.so (declared in include/dms.h): cache
+// lifetime, argument checks, kernel dispatch.  All compute runs in the
+// kernels of append.cuh and decode.cuh; this file only validates, allocates
+// at creation time and launches.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <unordered_set>
+
+#include "append.cuh"
+#include "decode.cuh"
+#include "dms.h"
+
+struct dms_cache {
+  int B, H, cap, D, w, NH;
+  int64_t t;
+  int device;
+  int num_sms;
+  dms::CacheView view;
+  float* part_acc;
+  float* part_ml;
+  int32_t* head_cnt;
+  size_t part_entries;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+std::mutex g_mu;
+std::unordered_set<const dms_cache*> g_live;
+thread_local int g_last_error = DMS_OK;
+
+bool is_live(const dms_cache* c) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return c != nullptr && g_live.count(c) != 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Make the cache's device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      ok = false;
+      return;
+    }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+// Is `p` device memory of device `dev` (or managed memory)?
+bool device_pointer_ok(const void* p, int dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (at.type == cudaMemoryTypeManaged) return true;
+  return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
+int launch_status() { return cudaGetLastError() == cudaSuccess ? DMS_OK : DMS_ERR_CUDA; }
+
+template <int D, int G>
+int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaStream_t st) {
+  using Sh = dms::DecodeShape<D, G>;
+  static bool attr_done[64] = {};
+  if (c->device < 64 && !attr_done[c->device]) {
+    if (cudaFuncSetAttribute(dms::decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) !=
+        cudaSuccess)
+      return DMS_ERR_CUDA;
+    attr_done[c->device] = true;
+  }
+  if (static_cast<int64_t>(c->NH + 1) * 4 > Sh::SMEM) return DMS_ERR_INVALID_ARG;
+  // Upper bound of the retained slots (the exact sum lives on the device).
+  const int64_t smax = static_cast<int64_t>(c->NH) * std::min<int64_t>(c->t, c->cap);
+  const int64_t want = (smax + int64_t(dms::kMinSlotsPerWarp) * Sh::NW - 1) / (int64_t(dms::kMinSlotsPerWarp) * Sh::NW);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(c->num_sms, want)));
+  if (static_cast<size_t>(grid) * Sh::NW + c->NH > c->part_entries) return DMS_ERR_INVALID_ARG;
+  dms::DecodeArgs a;
+  a.K = c->view.K;
+  a.V = c->view.V;
+  a.len = c->view.len;
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = out;
+  a.part_acc = c->part_acc;
+  a.part_ml = c->part_ml;
+  a.head_cnt = c->head_cnt;
+  a.err = c->view.err;
+  a.NH = c->NH;
+  a.Hkv = c->H;
+  a.cap = c->cap;
+  a.qscale = scale * 1.4426950408889634f;  // log2(e): softmax evaluated as 2^(x log2 e)
+  dms::decode_kernel<D, G><<<grid, Sh::NW * 32, Sh::SMEM, st>>>(a);
+  return launch_status();
+}
+
+template <int D>
+int launch_decode_d(dms_cache* c, const void* q, float* out, float scale, int G, cudaStream_t st) {
+  switch (G) {
+    case 1: return launch_decode_t<D, 1>(c, q, out, scale, st);
+    case 2: return launch_decode_t<D, 2>(c, q, out, scale, st);
+    case 3: return launch_decode_t<D, 3>(c, q, out, scale, st);
+    case 4: return launch_decode_t<D, 4>(c, q, out, scale, st);
+    case 5: return launch_decode_t<D, 5>(c, q, out, scale, st);
+    case 6: return launch_decode_t<D, 6>(c, q, out, scale, st);
+    case 7: return launch_decode_t<D, 7>(c, q, out, scale, st);
+    case 8: return launch_decode_t<D, 8>(c, q, out, scale, st);
+    default: return DMS_ERR_INVALID_ARG;
+  }
+}
+
+void free_cache_memory(dms_cache* c) {
+  cudaFree(c->view.K);
+  cudaFree(c->view.V);
+  cudaFree(c->view.slot_pos);
+  cudaFree(c->view.ring_slot);
+  cudaFree(c->view.ring_flag);
+  cudaFree(c->view.len);
+  cudaFree(c->view.err);
+  cudaFree(c->part_acc);
+  cudaFree(c->part_ml);
+  cudaFree(c->head_cnt);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dms_last_error(void) { return g_last_error; }
+
+const char* dms_error_string(int code) {
+  switch (code) {
+    case DMS_OK: return "ok";
+    case DMS_ERR_INVALID_ARG: return "invalid argument";
+    case DMS_ERR_CUDA: return "CUDA error";
+    case DMS_ERR_CAPACITY: return "cache capacity exceeded (sticky)";
+    case DMS_ERR_BAD_HANDLE: return "bad cache handle";
+    case DMS_ERR_TIMEOUT: return "device wait timed out (sticky)";
+    case DMS_ERR_EMPTY: return "cache is empty";
+    default: return "unknown error";
+  }
+}
+
+dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_dim, int window) {
+  g_last_error = DMS_OK;
+  if (batch < 1 || kv_heads < 1 || capacity < 1 || window < 1 || (head_dim != 64 && head_dim != 128)) {
+    g_last_error = DMS_ERR_INVALID_ARG;
+    return nullptr;
+  }
+  const int64_t NH = static_cast<int64_t>(batch) * kv_heads;
+  if (NH > (1 << 20) || NH * static_cast<int64_t>(capacity) >= (int64_t(1) << 31) ||
+      NH * static_cast<int64_t>(window) >= (int64_t(1) << 31)) {
+    g_last_error = DMS_ERR_INVALID_ARG;
+    return nullptr;
+  }
+  dms_cache* c = new (std::nothrow) dms_cache();
+  if (!c) {
+    g_last_error = DMS_ERR_CUDA;
+    return nullptr;
+  }
+  std::memset(c, 0, sizeof(*c));
+  c->B = batch;
+  c->H = kv_heads;
+  c->cap = capacity;
+  c->D = head_dim;
+  c->w = window;
+  c->NH = static_cast<int>(NH);
+  c->t = 0;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    g_last_error = DMS_ERR_CUDA;
+    return nullptr;
+  }
+  const size_t pool = static_cast<size_t>(NH) * capacity * head_dim * 2;
+  const size_t nslot = static_cast<size_t>(NH) * capacity;
+  const size_t nring = static_cast<size_t>(NH) * window;
+  constexpr int kNWMax = 4;  // warps per CTA of the decode kernel
+  c->part_entries = static_cast<size_t>(c->num_sms) * kNWMax + NH;
+  const size_t part_acc = c->part_entries * DMS_MAX_GROUP * head_dim * sizeof(float);
+  const size_t part_ml = c->part_entries * DMS_MAX_GROUP * 2 * sizeof(float);
+  bool ok = cudaMalloc(&c->view.K, pool) == cudaSuccess && cudaMalloc(&c->view.V, pool) == cudaSuccess &&
+            cudaMalloc(&c->view.slot_pos, nslot * 4) == cudaSuccess &&
+            cudaMalloc(&c->view.ring_slot, nring * 4) == cudaSuccess &&
+            cudaMalloc(&c->view.ring_flag, nring) == cudaSuccess &&
+            cudaMalloc(&c->view.len, NH * 4) == cudaSuccess && cudaMalloc(&c->view.err, kAlign) == cudaSuccess &&
+            cudaMalloc(&c->part_acc, part_acc) == cudaSuccess && cudaMalloc(&c->part_ml, part_ml) == cudaSuccess &&
+            cudaMalloc(&c->head_cnt, NH * 4) == cudaSuccess;
+  ok = ok && cudaMemset(c->view.K, 0, pool) == cudaSuccess && cudaMemset(c->view.V, 0, pool) == cudaSuccess &&
+       cudaMemset(c->view.slot_pos, 0xff, nslot * 4) == cudaSuccess &&
+       cudaMemset(c->view.ring_slot, 0xff, nring * 4) == cudaSuccess &&
+       cudaMemset(c->view.ring_flag, 0, nring) == cudaSuccess && cudaMemset(c->view.len, 0, NH * 4) == cudaSuccess &&
+       cudaMemset(c->view.err, 0, kAlign) == cudaSuccess && cudaMemset(c->head_cnt, 0, NH * 4) == cudaSuccess &&
+       cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    free_cache_memory(c);
+    delete c;
+    g_last_error = DMS_ERR_CUDA;
+    return nullptr;
+  }
+  c->view.NH = c->NH;
+  c->view.cap = capacity;
+  c->view.D = head_dim;
+  c->view.w = window;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_live.insert(c);
+  }
+  return c;
+}
+
+void dms_cache_destroy(dms_cache_t* cache) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (cache == nullptr || g_live.erase(cache) == 0) return;
+  }
+  DeviceGuard g(cache->device);
+  cudaDeviceSynchronize();
+  free_cache_memory(cache);
+  delete cache;
+}
+
+int64_t dms_cache_position(dms_cache_t* cache) { return is_live(cache) ? cache->t : -1; }
+
+int dms_append(dms_cache_t* c, const void* k, const void* v, const float* evict_logit, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  if (!k || !v || !evict_logit || !aligned16(k) || !aligned16(v) || !aligned16(evict_logit))
+    return DMS_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return DMS_ERR_CUDA;
+  if (!device_pointer_ok(k, c->device) || !device_pointer_ok(v, c->device) ||
+      !device_pointer_ok(evict_logit, c->device))
+    return DMS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int threads = 256;
+  const int blocks = (c->NH * 32 + threads - 1) / threads;
+  if (c->D == 128)
+    dms::append_kernel<128><<<blocks, threads, 0, st>>>(c->view, static_cast<const uint4*>(k),
+                                                        static_cast<const uint4*>(v), evict_logit, c->t);
+  else
+    dms::append_kernel<64><<<blocks, threads, 0, st>>>(c->view, static_cast<const uint4*>(k),
+                                                       static_cast<const uint4*>(v), evict_logit, c->t);
+  const int rc = launch_status();
+  if (rc == DMS_OK) c->t += 1;
+  return rc;
+}
+
+int dms_append_chunk(dms_cache_t* c, const void* k, const void* v, const float* logits, int chunk, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  if (chunk < 1 || !k || !v || !logits || !aligned16(k) || !aligned16(v) || !aligned16(logits))
+    return DMS_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return DMS_ERR_CUDA;
+  if (!device_pointer_ok(k, c->device) || !device_pointer_ok(v, c->device) || !device_pointer_ok(logits, c->device))
+    return DMS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int blocks = (c->NH + 3) / 4;
+  if (c->D == 128)
+    dms::append_chunk_kernel<128><<<blocks, 128, 0, st>>>(c->view, static_cast<const uint4*>(k),
+                                                          static_cast<const uint4*>(v), logits, c->t, chunk);
+  else
+    dms::append_chunk_kernel<64><<<blocks, 128, 0, st>>>(c->view, static_cast<const uint4*>(k),
+                                                         static_cast<const uint4*>(v), logits, c->t, chunk);
+  const int rc = launch_status();
+  if (rc == DMS_OK) c->t += chunk;
+  return rc;
+}
+
+int dms_decode_attention(dms_cache_t* c, const void* q, float* out, float scale, int q_heads, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  if (!q || !out || !aligned16(q) || !aligned16(out) || q_heads < 1 || q_heads % c->H != 0 ||
+      q_heads / c->H > DMS_MAX_GROUP || !std::isfinite(scale))
+    return DMS_ERR_INVALID_ARG;
+  if (c->t == 0) return DMS_ERR_EMPTY;
+  DeviceGuard g(c->device);
+  if (!g.ok) return DMS_ERR_CUDA;
+  if (!device_pointer_ok(q, c->device) || !device_pointer_ok(out, c->device)) return DMS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int G = q_heads / c->H;
+  return c->D == 128 ? launch_decode_d<128>(c, q, out, scale, G, st) : launch_decode_d<64>(c, q, out, scale, G, st);
+}
+
+int dms_cache_lengths(dms_cache_t* c, int32_t* out_dev, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  if (!out_dev) return DMS_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!device_pointer_ok(out_dev, c->device)) return DMS_ERR_INVALID_ARG;
+  return cudaMemcpyAsync(out_dev, c->view.len, static_cast<size_t>(c->NH) * 4, cudaMemcpyDeviceToDevice,
+                         static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DMS_OK
+             : DMS_ERR_CUDA;
+}
+
+int dms_cache_slot_positions(dms_cache_t* c, int32_t* out_dev, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  if (!out_dev) return DMS_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!device_pointer_ok(out_dev, c->device)) return DMS_ERR_INVALID_ARG;
+  return cudaMemcpyAsync(out_dev, c->view.slot_pos, static_cast<size_t>(c->NH) * c->cap * 4,
+                         cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DMS_OK
+             : DMS_ERR_CUDA;
+}
+
+int dms_cache_export_kv(dms_cache_t* c, void* k_out, void* v_out, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  if (!k_out || !v_out || !aligned16(k_out) || !aligned16(v_out)) return DMS_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!device_pointer_ok(k_out, c->device) || !device_pointer_ok(v_out, c->device)) return DMS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int blocks = c->num_sms * 8;
+  if (c->D == 128)
+    dms::export_kv_kernel<128><<<blocks, 256, 0, st>>>(c->view, static_cast<uint4*>(k_out), static_cast<uint4*>(v_out));
+  else
+    dms::export_kv_kernel<64><<<blocks, 256, 0, st>>>(c->view, static_cast<uint4*>(k_out), static_cast<uint4*>(v_out));
+  return launch_status();
+}
+
+int dms_cache_status(dms_cache_t* c, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  DeviceGuard g(c->device);
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DMS_ERR_CUDA;
+  int32_t bits = 0;
+  if (cudaMemcpy(&bits, c->view.err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return DMS_ERR_CUDA;
+  if (bits & dms::kErrBitTimeout) return DMS_ERR_TIMEOUT;
+  if (bits & dms::kErrBitCapacity) return DMS_ERR_CAPACITY;
+  return DMS_OK;
+}
+
+}  // extern "C"

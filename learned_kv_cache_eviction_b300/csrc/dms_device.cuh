@@ -1,0 +1,114 @@
+// dms_device.cuh -- device-side helpers shared by the DMS kernels:
+// mbarrier / bulk-copy wrappers (inline PTX for sm_103a), warp reductions,
+// bf16 unpacking, and the view of the cache's device state.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dms {
+
+// Sticky device error bits (the host maps them to DMS_ERR_* codes).
+constexpr int kErrBitCapacity = 1;
+constexpr int kErrBitTimeout = 2;
+
+// Time limit of every device-side wait on an mbarrier (ns of %globaltimer).
+constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;
+
+// Device state of one cache.  K is stored with a per-slot permutation of the
+// 16-byte chunks of each row (chunk c of slot s lives at chunk c ^ (s & 7)),
+// so that a contiguous bulk copy of consecutive slots into shared memory can
+// be read one row per lane without bank conflicts.  V is stored unpermuted.
+struct CacheView {
+  uint4* K;            // [NH][cap][D/8] 16-byte chunks (bf16 x 8)
+  uint4* V;            // [NH][cap][D/8]
+  int32_t* slot_pos;   // [NH][cap]
+  int32_t* ring_slot;  // [NH][w]
+  uint8_t* ring_flag;  // [NH][w]
+  int32_t* len;        // [NH]
+  int32_t* err;        // sticky error bits
+  int NH, cap, D, w;
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false after the time
+// limit (the caller latches kErrBitTimeout and stops).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// One bulk (non-tensor) asynchronous copy global -> shared, completing on `bar`
+// with `bytes` transaction bytes.  dst, src 16-byte aligned; bytes % 16 == 0.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 2^x (PTX ex2.approx, flush-to-zero; ex2(-inf) = +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two bf16 packed in a 32-bit word (element 2j in the low half) -> float2.
+// Widening bf16 to fp32 is exact: the bf16 bits become the top half.
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+}  // namespace dms

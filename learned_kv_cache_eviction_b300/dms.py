@@ -1,0 +1,224 @@
+"""Python binding of libdms.so (the C ABI in include/dms.h).
+
+Argument marshalling only: tensors are checked (dtype, device, shape,
+contiguity) and passed as raw device pointers with the current CUDA stream.
+Every step of the method runs in the library's CUDA kernels.  If libdms.so is
+missing this module raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+DMS_OK = 0
+DMS_ERR_INVALID_ARG = -1
+DMS_ERR_CUDA = -2
+DMS_ERR_CAPACITY = -3
+DMS_ERR_BAD_HANDLE = -4
+DMS_ERR_TIMEOUT = -5
+DMS_ERR_EMPTY = -6
+DMS_MAX_GROUP = 8
+
+# Entry points declared in include/dms.h: name -> (restype, argtypes)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+SIGNATURES = {
+    "dms_cache_create": (_P, [_I, _I, _I, _I, _I]),
+    "dms_last_error": (_I, []),
+    "dms_cache_destroy": (None, [_P]),
+    "dms_append": (_I, [_P, _P, _P, _P, _P]),
+    "dms_append_chunk": (_I, [_P, _P, _P, _P, _I, _P]),
+    "dms_decode_attention": (_I, [_P, _P, _P, ctypes.c_float, _I, _P]),
+    "dms_cache_lengths": (_I, [_P, _P, _P]),
+    "dms_cache_slot_positions": (_I, [_P, _P, _P]),
+    "dms_cache_export_kv": (_I, [_P, _P, _P, _P]),
+    "dms_cache_status": (_I, [_P, _P]),
+    "dms_cache_position": (ctypes.c_int64, [_P]),
+    "dms_error_string": (ctypes.c_char_p, [_I]),
+}
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libdms.so (built in-tree) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m learned_kv_cache_eviction_b300.build` "
+            "(the DMS kernels have no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+class DmsError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        msg = load_library().dms_error_string(code).decode()
+        super().__init__(f"{what}: {msg} ({code})" if what else f"{msg} ({code})")
+
+
+def _check(code: int, what: str) -> None:
+    if code != DMS_OK:
+        raise DmsError(code, what)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape, device) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class DmsCache:
+    """A DMS compacted KV cache for one attention layer (all device state is
+    owned by libdms.so)."""
+
+    def __init__(self, batch: int, kv_heads: int, capacity: int, head_dim: int, window: int = 16,
+                 device=None):
+        self._lib = load_library()
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None
+                                   else torch.device(device).index or 0)
+        with torch.cuda.device(self.device):
+            h = self._lib.dms_cache_create(batch, kv_heads, capacity, head_dim, window)
+        if not h:
+            raise DmsError(self._lib.dms_last_error(), "dms_cache_create")
+        self._h = ctypes.c_void_p(h)
+        self.batch, self.kv_heads, self.capacity, self.head_dim, self.window = (
+            batch, kv_heads, capacity, head_dim, window)
+
+    # -- lifetime -----------------------------------------------------------
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.dms_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if self._h is None:
+            raise DmsError(DMS_ERR_BAD_HANDLE, "cache is closed")
+        return self._h
+
+    @property
+    def position(self) -> int:
+        return int(self._lib.dms_cache_position(self.handle))
+
+    # -- hot path ------------------------------------------------------------
+    def append(self, k: torch.Tensor, v: torch.Tensor, evict_logit: torch.Tensor, stream=None) -> None:
+        B, H, D = self.batch, self.kv_heads, self.head_dim
+        _need(k, "k", torch.bfloat16, (B, H, D), self.device)
+        _need(v, "v", torch.bfloat16, (B, H, D), self.device)
+        _need(evict_logit, "evict_logit", torch.float32, (B, H), self.device)
+        _check(self._lib.dms_append(self.handle, k.data_ptr(), v.data_ptr(), evict_logit.data_ptr(),
+                                    _stream_handle(stream)), "dms_append")
+
+    def append_chunk(self, k: torch.Tensor, v: torch.Tensor, logits: torch.Tensor, stream=None) -> None:
+        B, H, D = self.batch, self.kv_heads, self.head_dim
+        C = k.shape[2] if k.dim() == 4 else -1
+        _need(k, "k", torch.bfloat16, (B, H, C, D), self.device)
+        _need(v, "v", torch.bfloat16, (B, H, C, D), self.device)
+        _need(logits, "logits", torch.float32, (B, H, C), self.device)
+        _check(self._lib.dms_append_chunk(self.handle, k.data_ptr(), v.data_ptr(), logits.data_ptr(), C,
+                                          _stream_handle(stream)), "dms_append_chunk")
+
+    def decode_attention(self, q: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,
+                         stream=None) -> torch.Tensor:
+        B, D = self.batch, self.head_dim
+        if q.dim() != 3:
+            raise ValueError("q must be [batch][q_heads][head_dim]")
+        Hq = q.shape[1]
+        _need(q, "q", torch.bfloat16, (B, Hq, D), self.device)
+        if out is None:
+            out = torch.empty((B, Hq, D), dtype=torch.float32, device=self.device)
+        _need(out, "out", torch.float32, (B, Hq, D), self.device)
+        scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+        _check(self._lib.dms_decode_attention(self.handle, q.data_ptr(), out.data_ptr(), scale, Hq,
+                                              _stream_handle(stream)), "dms_decode_attention")
+        return out
+
+    # -- state export ----------------------------------------------------------
+    def lengths(self, stream=None) -> torch.Tensor:
+        out = torch.empty((self.batch, self.kv_heads), dtype=torch.int32, device=self.device)
+        _check(self._lib.dms_cache_lengths(self.handle, out.data_ptr(), _stream_handle(stream)), "dms_cache_lengths")
+        return out
+
+    def slot_positions(self, stream=None) -> torch.Tensor:
+        out = torch.empty((self.batch, self.kv_heads, self.capacity), dtype=torch.int32, device=self.device)
+        _check(self._lib.dms_cache_slot_positions(self.handle, out.data_ptr(), _stream_handle(stream)),
+               "dms_cache_slot_positions")
+        return out
+
+    def export_kv(self, stream=None):
+        shp = (self.batch, self.kv_heads, self.capacity, self.head_dim)
+        k = torch.empty(shp, dtype=torch.bfloat16, device=self.device)
+        v = torch.empty(shp, dtype=torch.bfloat16, device=self.device)
+        _check(self._lib.dms_cache_export_kv(self.handle, k.data_ptr(), v.data_ptr(), _stream_handle(stream)),
+               "dms_cache_export_kv")
+        return k, v
+
+    def status(self, stream=None) -> int:
+        """Synchronize the stream and return the sticky device status code."""
+        return int(self._lib.dms_cache_status(self.handle, _stream_handle(stream)))
+
+
+# Module-level aliases carrying the C entry-point names.
+def dms_cache_create(batch, kv_heads, capacity, head_dim, window=16, device=None) -> DmsCache:
+    return DmsCache(batch, kv_heads, capacity, head_dim, window, device)
+
+
+def dms_append(cache: DmsCache, k, v, evict_logit, stream=None) -> None:
+    cache.append(k, v, evict_logit, stream)
+
+
+def dms_append_chunk(cache: DmsCache, k, v, logits, stream=None) -> None:
+    cache.append_chunk(k, v, logits, stream)
+
+
+def dms_decode_attention(cache: DmsCache, q, out=None, scale=None, stream=None):
+    return cache.decode_attention(q, out, scale, stream)
+
+
+def dms_cache_lengths(cache: DmsCache, stream=None):
+    return cache.lengths(stream)
+
+
+def dms_cache_slot_positions(cache: DmsCache, stream=None):
+    return cache.slot_positions(stream)
+
+
+def dms_cache_status(cache: DmsCache, stream=None) -> int:
+    return cache.status(stream)
+
+
+def dms_cache_destroy(cache: DmsCache) -> None:
+    cache.close()

@@ -183,31 +183,25 @@ class SlotSimulator:
         self.overflow = False
 
     def append(self, e_t) -> np.ndarray:
-        """Append token ``self.t`` for every (b, h); returns its slot (-1 if
-        it overflowed the capacity)."""
+        """Append token ``self.t`` to every (b, h); returns its slot per head
+        (-1 where it overflowed the capacity).  Heads are independent, so the
+        rule is applied to all of them at once."""
         e_t = np.asarray(e_t, dtype=bool).reshape(self.B, self.H)
         t, w = self.t, self.w
         r = t % w
-        slots = np.empty((self.B, self.H), dtype=np.int64)
-        for b in range(self.B):
-            for h in range(self.H):
-                if t >= w and self.ring_flag[b, h, r]:
-                    s = int(self.ring_slot[b, h, r])  # t - w leaves, t takes its slot
-                else:
-                    s = int(self.len[b, h])
-                    if s >= self.cap:
-                        self.overflow = True
-                        self.ring_slot[b, h, r] = -1
-                        self.ring_flag[b, h, r] = False
-                        slots[b, h] = -1
-                        continue
-                    self.len[b, h] = s + 1
-                self.slot_pos[b, h, s] = t
-                self.ring_slot[b, h, r] = s
-                self.ring_flag[b, h, r] = bool(e_t[b, h])
-                slots[b, h] = s
+        retire = (t >= w) & self.ring_flag[:, :, r]      # token t - w was marked: it leaves now
+        s = np.where(retire, self.ring_slot[:, :, r], self.len)  # ... and t takes its slot
+        over = ~retire & (self.len >= self.cap)
+        self.len = self.len + (~retire & ~over)
+        s = np.where(over, -1, s)
+        bi, hi = np.nonzero(s >= 0)
+        self.slot_pos[bi, hi, s[bi, hi]] = t
+        self.ring_slot[:, :, r] = s
+        self.ring_flag[:, :, r] = e_t & (s >= 0)
+        if over.any():
+            self.overflow = True
         self.t = t + 1
-        return slots
+        return s
 
     def append_chunk(self, e_chunk) -> np.ndarray:
         """``e_chunk [B][Hkv][C]``: C appends in position order."""

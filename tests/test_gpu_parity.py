@@ -1,0 +1,299 @@
+"""GPU parity: libdms.so against the CPU oracle on identical seeded inputs.
+
+Bar (stated for the method's decode path): eviction bookkeeping -- which
+token occupies which slot, per-head lengths, stored K/V bytes -- bit-exact;
+attention outputs within max-abs 1e-2 and mean relative error
+sum|gpu - ref| / sum|ref| <= 1e-3 against the float64 oracle.  A tighter bar
+derived from the fp32 arithmetic of the kernel (max-abs 1e-4, mean relative
+1e-4) is asserted as well, so that one dropped or duplicated key
+in a 2000-key head cannot hide under the looser one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.dms_oracle as O
+from learned_kv_cache_eviction_b300 import dms, workload as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_STATED = (1e-2, 1e-3)
+TOL_TIGHT = (1e-4, 1e-4)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    dms.load_library()
+
+
+def errors(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    d = np.abs(got - ref)
+    return float(d.max()), float(d.sum() / np.abs(ref).sum())
+
+
+def assert_attention_close(got, ref, what=""):
+    mx, rel = errors(got, ref)
+    assert mx <= TOL_STATED[0] and rel <= TOL_STATED[1], f"{what}: max-abs {mx:.3e} mean-rel {rel:.3e}"
+    assert mx <= TOL_TIGHT[0] and rel <= TOL_TIGHT[1], f"{what}: max-abs {mx:.3e} mean-rel {rel:.3e}"
+    return mx, rel
+
+
+class Trajectory:
+    """Drives one cache and the oracle's slot simulator through the same
+    appends, and checks the bookkeeping bit-exactly."""
+
+    def __init__(self, wl: W.Workload, T: int, layer: int = 0, rows=None):
+        self.wl, self.layer, self.T = wl, layer, T
+        k, v, lg = W.kv_range(wl, layer, 0, T)
+        self.k, self.v, self.lg = k, v, lg
+        self.e = O.eviction_decisions(lg.numpy())
+        self.rows = list(range(wl.B)) if rows is None else list(rows)
+        self.k_np = k[self.rows].float().numpy()
+        self.v_np = v[self.rows].float().numpy()
+        self.cache = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
+        self.sim = O.SlotSimulator(wl.B, wl.Hkv, wl.cap, wl.w)
+        self.t = 0
+
+    def append_chunk(self, n):
+        sl = slice(self.t, self.t + n)
+        self.cache.append_chunk(self.k[:, :, sl].contiguous().cuda(), self.v[:, :, sl].contiguous().cuda(),
+                                self.lg[:, :, sl].contiguous().cuda())
+        self.sim.append_chunk(self.e[:, :, sl])
+        self.t += n
+
+    def append(self):
+        t = self.t
+        self.cache.append(self.k[:, :, t].contiguous().cuda(), self.v[:, :, t].contiguous().cuda(),
+                          self.lg[:, :, t].contiguous().cuda())
+        self.sim.append(self.e[:, :, t])
+        self.t += 1
+
+    def check_lengths(self):
+        got = self.cache.lengths().cpu().numpy()
+        assert np.array_equal(got, self.sim.len), f"lengths differ at t={self.t}"
+
+    def check_slots(self):
+        got = self.cache.slot_positions().cpu().numpy()
+        assert np.array_equal(got, self.sim.slot_pos), f"slot map differs at t={self.t}"
+
+    def check_kv(self):
+        kk, vv = self.cache.export_kv()
+        kk, vv = kk.cpu(), vv.cpu()
+        sp = self.sim.slot_pos
+        for b in range(self.wl.B):
+            for h in range(self.wl.Hkv):
+                n = int(self.sim.len[b, h])
+                pos = torch.from_numpy(sp[b, h, :n].astype(np.int64))
+                assert torch.equal(kk[b, h, :n], self.k[b, h, pos]), (b, h)
+                assert torch.equal(vv[b, h, :n], self.v[b, h, pos]), (b, h)
+
+    def decode_and_compare(self, q, what=""):
+        """q: bf16 [B][Hq][D] (CPU) of the step just appended."""
+        out = self.cache.decode_attention(q.cuda(), scale=self.wl.scale)
+        assert self.cache.status() == dms.DMS_OK
+        got = out.cpu().numpy()[self.rows]
+        ref = O.decode_attention(q[self.rows].float().numpy(), self.k_np, self.v_np, self.e[self.rows],
+                                 self.t - 1, self.wl.w, self.wl.scale)
+        return assert_attention_close(got, ref, f"{what} t={self.t - 1}")
+
+
+def _small(name, B, Hq, Hkv, D, w, cap, logits, seed=11):
+    return W.Workload(name, B=B, Hq=Hq, Hkv=Hkv, D=D, w=w, cap=cap, seed=seed, logits=logits)
+
+
+def test_tiny_every_step():
+    """The tiny workload (B1, Hq4/Hkv2, d64, 256 steps from empty): bookkeeping,
+    stored bytes and attention at every step."""
+    wl = W.WORKLOADS["tiny"]
+    tr = Trajectory(wl, wl.decode)
+    q = W.q_range(wl, 0, 0, wl.decode)
+    for t in range(wl.decode):
+        tr.append()
+        tr.check_lengths()
+        tr.check_slots()
+        tr.decode_and_compare(q[:, :, t].contiguous(), "tiny")
+    tr.check_kv()
+
+
+@pytest.mark.parametrize("case", [
+    # name, B, Hq, Hkv, D, w, cap, logits, T
+    ("mha-d128", 2, 3, 3, 128, 16, 300, ("normal", 0.0, 1.0), 300),
+    ("g3-d64", 3, 6, 2, 64, 16, 200, ("normal", 0.5, 1.0), 200),
+    ("g5-d128", 2, 10, 2, 128, 16, 260, ("normal", 1.15, 1.0), 260),
+    ("g8-d128", 1, 64, 8, 128, 16, 200, ("normal", 2.0, 1.5), 200),
+    ("g7-d64", 1, 14, 2, 64, 4, 130, ("normal", 0.3, 2.0), 130),
+    ("eager-w1", 2, 8, 2, 128, 1, 150, ("normal", 0.0, 1.0), 150),
+    ("short-T-below-w", 2, 8, 2, 64, 16, 16, ("normal", 1.0, 1.0), 10),
+    ("all-keep", 2, 8, 2, 128, 16, 400, ("const", -10.0), 400),
+    ("all-evict-window", 2, 8, 2, 128, 16, 16, ("const", 10.0), 300),
+    ("many-short-heads", 40, 16, 8, 64, 16, 70, ("normal", 1.0, 1.0), 70),
+])
+def test_edge_shapes(case):
+    name, B, Hq, Hkv, D, w, cap, logits, T = case
+    wl = _small(name, B, Hq, Hkv, D, w, cap, logits)
+    tr = Trajectory(wl, T)
+    q = W.q_range(wl, 0, 0, T)
+    check_at = set(range(0, T, max(1, T // 25))) | {T - 1}
+    for t in range(T):
+        tr.append()
+        if t in check_at:
+            tr.check_lengths()
+            tr.decode_and_compare(q[:, :, t].contiguous(), name)
+    tr.check_slots()
+    tr.check_kv()
+
+
+def test_first_step_returns_first_value_exactly():
+    wl = _small("t0", 2, 8, 2, 128, 16, 8, ("normal", 0.0, 1.0))
+    tr = Trajectory(wl, 1)
+    tr.append()
+    q = W.q_range(wl, 0, 0, 1)[:, :, 0].contiguous()
+    out = tr.cache.decode_attention(q.cuda(), scale=wl.scale).cpu()
+    expect = tr.v[:, :, 0].float().repeat_interleave(wl.G, dim=1)
+    assert torch.equal(out, expect)
+
+
+@pytest.mark.parametrize("chunk", [1, 7, 16, 33, 100])
+def test_chunk_append_equals_single_appends(chunk):
+    wl = _small("chunk", 3, 8, 4, 64, 16, 400, ("normal", 0.8, 1.0), seed=5)
+    T = 350
+    a = Trajectory(wl, T)
+    b = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
+    while a.t < T:
+        n = min(chunk, T - a.t)
+        t0 = a.t
+        a.append_chunk(n)
+        for t in range(t0, t0 + n):
+            b.append(a.k[:, :, t].contiguous().cuda(), a.v[:, :, t].contiguous().cuda(),
+                     a.lg[:, :, t].contiguous().cuda())
+    a.check_lengths()
+    a.check_slots()
+    assert torch.equal(a.cache.lengths(), b.lengths())
+    assert torch.equal(a.cache.slot_positions(), b.slot_positions())
+    ka, va = a.cache.export_kv()
+    kb, vb = b.export_kv()
+    assert torch.equal(ka, kb) and torch.equal(va, vb)
+    a.check_kv()
+    assert b.position == a.cache.position == T
+
+
+def test_capacity_overflow_is_reported():
+    wl = _small("cap", 1, 4, 2, 64, 4, 10, ("const", -10.0))
+    tr = Trajectory(wl, 14)
+    for _ in range(10):
+        tr.append()
+    assert tr.cache.status() == dms.DMS_OK
+    tr.append()
+    assert tr.cache.status() == dms.DMS_ERR_CAPACITY
+    assert tr.sim.overflow
+    tr.append()
+    tr.check_lengths()
+    tr.check_slots()
+    assert tr.cache.status() == dms.DMS_ERR_CAPACITY  # sticky
+
+
+def test_host_side_argument_errors():
+    c = dms.DmsCache(2, 2, 32, 64, 16)
+    q = torch.zeros(2, 4, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dms.DmsError) as ei:
+        c.decode_attention(q)
+    assert ei.value.code == dms.DMS_ERR_EMPTY
+    lib = dms.load_library()
+    k = torch.zeros(2, 2, 64, dtype=torch.bfloat16, device="cuda")
+    lg = torch.zeros(2, 2, dtype=torch.float32, device="cuda")
+    c.append(k, k, lg)
+    out = torch.empty(2, 4, 64, dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    h = c.handle
+    assert lib.dms_decode_attention(h, q.data_ptr(), out.data_ptr(), 0.1, 3, s) == dms.DMS_ERR_INVALID_ARG
+    assert lib.dms_decode_attention(h, q.data_ptr(), out.data_ptr(), 0.1, 2 * 9, s) == dms.DMS_ERR_INVALID_ARG
+    assert lib.dms_decode_attention(h, q.data_ptr() + 2, out.data_ptr(), 0.1, 4, s) == dms.DMS_ERR_INVALID_ARG
+    assert lib.dms_decode_attention(h, q.data_ptr(), out.data_ptr(), float("nan"), 4, s) == dms.DMS_ERR_INVALID_ARG
+    host = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
+    assert lib.dms_decode_attention(h, host.data_ptr(), out.data_ptr(), 0.1, 4, s) == dms.DMS_ERR_INVALID_ARG
+    assert lib.dms_append_chunk(h, k.data_ptr(), k.data_ptr(), lg.data_ptr(), 0, s) == dms.DMS_ERR_INVALID_ARG
+    assert c.position == 1  # nothing was enqueued by the failed calls
+    assert lib.dms_decode_attention(h, q.data_ptr(), out.data_ptr(), 0.1, 4, s) == dms.DMS_OK
+    assert c.status() == dms.DMS_OK
+    c.close()
+    with pytest.raises(dms.DmsError):
+        c.decode_attention(q)
+
+
+def _prefill_then_decode(wl, T_prefill, n_decode, rows, layer=0, check_kv=False):
+    T = T_prefill + n_decode
+    tr = Trajectory(wl, T, layer=layer, rows=rows)
+    while tr.t < T_prefill:
+        tr.append_chunk(min(wl.chunk, T_prefill - tr.t))
+    tr.check_lengths()
+    q = W.q_range(wl, layer, T_prefill, T)
+    worst = (0.0, 0.0)
+    for j in range(n_decode):
+        tr.append()
+        tr.check_lengths()
+        mx, rel = tr.decode_and_compare(q[:, :, j].contiguous(), wl.name)
+        worst = (max(worst[0], mx), max(worst[1], rel))
+    tr.check_slots()
+    if check_kv:
+        tr.check_kv()
+    return tr, worst
+
+
+def test_llama_prefill_and_decode_sampled():
+    """Llama-3.2-1B-like: 3584-token chunked fill (C=512) + 512 decode steps;
+    bookkeeping every step, attention every 32nd step on rows {0, B-1}."""
+    wl = W.WORKLOADS["llama-3.2-1b"]
+    rows = [0, wl.B - 1]
+    T0 = wl.prefill
+    tr = Trajectory(wl, T0 + wl.decode, rows=rows)
+    while tr.t < T0:
+        tr.append_chunk(min(wl.chunk, T0 - tr.t))
+    q = W.q_range(wl, 0, T0, T0 + wl.decode)
+    for j in range(wl.decode):
+        tr.append()
+        tr.check_lengths()
+        if j % 32 == 0 or j == wl.decode - 1:
+            tr.decode_and_compare(q[:, :, j].contiguous(), wl.name)
+    tr.check_slots()
+    tr.check_kv()
+
+
+def test_qwen3_8b_full_size_cr8_and_cr1():
+    """The benchmark's workload at full size (B32, Hq32/Hkv8, d128, n=16384):
+    the kernel runs in the same launch configuration as the benchmark; outputs
+    are sampled on rows {0, 31} at the last 4 steps; bookkeeping of all rows
+    is bit-exact."""
+    for name in ("qwen3-8b", "qwen3-8b-cr1"):
+        wl = W.WORKLOADS[name]
+        tr, worst = _prefill_then_decode(wl, wl.cap - 4, 4, rows=[0, wl.B - 1])
+        n = wl.cap
+        lens = tr.sim.len
+        if name == "qwen3-8b-cr1":
+            assert (lens == n).all()
+        else:
+            cr = n / lens.mean()
+            assert 7.0 < cr < 9.0, cr
+        del tr
+        torch.cuda.empty_cache()
+
+
+def test_qwen_r1_width_sampled():
+    """Qwen-R1-32B-like width scaling (B64, G=5, per-head eviction 50-97%):
+    a 4096-token history, rows {0, 63}."""
+    wl = W.WORKLOADS["qwen-r1-32b"].with_(chunk=512)
+    tr, _ = _prefill_then_decode(wl, 4092, 4, rows=[0, wl.B - 1])
+    lens = tr.sim.len
+    assert lens.max() > 3 * lens.min()  # strongly imbalanced heads
+
+
+def test_long_context_one_layer():
+    """Long-context stack, one of its 8 layers (B4, Hq64/Hkv8, d128): 32768-token
+    chunked fill + 4 decode steps, all rows."""
+    wl = W.WORKLOADS["long-context"]
+    _prefill_then_decode(wl, wl.prefill, 4, rows=list(range(wl.B)), layer=3)
