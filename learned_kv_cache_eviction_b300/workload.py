@@ -5,11 +5,13 @@ arithmetic (no decision threshold, no mask, no attention).  Tests feed the
 same tensors to the CUDA library and to the CPU oracle; the benchmark uses it
 for its inputs.
 
-Every tensor is a pure function of (workload seed, layer, kind, block): the
-positions of a sequence are cut into blocks of ``BLOCK`` tokens and each block
-of each kind of input gets its own ``torch.Generator`` seeded from a 64-bit
-mix of those integers.  So the inputs of position t do not depend on which
-other positions were drawn, or in which order.
+Every tensor is a pure function of (workload seed, layer, kind, block, batch
+row): the positions of a sequence are cut into blocks of ``BLOCK`` tokens and
+each (block, row) of each kind of input gets its own ``torch.Generator`` seeded
+from a 64-bit mix of those integers.  So the inputs of position t of row b do
+not depend on which other positions or rows were drawn, or in which order.
+(CPU and CUDA generators give different streams: tests draw on the CPU and
+upload; the benchmark may draw directly on the GPU.)
 
 Shapes and distributions follow the five synthetic workloads of the method's
 benchmark plan (Q/K/V ~ N(0,1) rounded to bf16, float32 eviction logits),
@@ -144,18 +146,13 @@ def head_logit_bias(wl: Workload, layer: int) -> np.ndarray:
     return mu.astype(np.float64)
 
 
-def kv_block(wl: Workload, layer: int, block: int, device="cpu"):
-    """Keys, values and eviction logits of positions [64*block, 64*block+64).
-
-    Returns ``k, v``: bf16 ``[B][Hkv][64][D]`` and ``logits``: float32
-    ``[B][Hkv][64]``, on ``device``.
-    """
-    shp = (wl.B, wl.Hkv, BLOCK, wl.D)
-    k = torch.randn(shp, generator=_gen(device, wl.seed, layer, _KIND_K, block),
+def _row_block_kv(wl: Workload, layer: int, block: int, b: int, device):
+    shp = (wl.Hkv, BLOCK, wl.D)
+    k = torch.randn(shp, generator=_gen(device, wl.seed, layer, _KIND_K, block, b),
                     device=device, dtype=torch.float32).to(torch.bfloat16)
-    v = torch.randn(shp, generator=_gen(device, wl.seed, layer, _KIND_V, block),
+    v = torch.randn(shp, generator=_gen(device, wl.seed, layer, _KIND_V, block, b),
                     device=device, dtype=torch.float32).to(torch.bfloat16)
-    z = torch.randn((wl.B, wl.Hkv, BLOCK), generator=_gen(device, wl.seed, layer, _KIND_LOGIT, block),
+    z = torch.randn((wl.Hkv, BLOCK), generator=_gen(device, wl.seed, layer, _KIND_LOGIT, block, b),
                     device=device, dtype=torch.float32)
     kind = wl.logits[0]
     if kind == "normal":
@@ -163,23 +160,38 @@ def kv_block(wl: Workload, layer: int, block: int, device="cpu"):
     elif kind == "const":
         lg = torch.full_like(z, float(wl.logits[1]))
     elif kind == "beta_head":
-        mu = torch.from_numpy(head_logit_bias(wl, layer)).to(device=device, dtype=torch.float32)
-        lg = z + mu[:, :, None]
+        mu = torch.from_numpy(head_logit_bias(wl, layer)[b]).to(device=device, dtype=torch.float32)
+        lg = z + mu[:, None]
     elif kind == "normal_forced_keep":
         lg = z * float(wl.logits[2]) + float(wl.logits[1])
-        u = torch.rand((wl.B, wl.Hkv, BLOCK), generator=_gen(device, wl.seed, layer, _KIND_FORCE, block),
+        u = torch.rand((wl.Hkv, BLOCK), generator=_gen(device, wl.seed, layer, _KIND_FORCE, block, b),
                        device=device, dtype=torch.float32)
         lg = torch.where(u < float(wl.logits[3]), torch.full_like(lg, -10.0), lg)
     else:
         raise ValueError(f"unknown logit distribution {kind!r}")
-    return k, v, lg.contiguous()
+    return k, v, lg
 
 
-def q_block(wl: Workload, layer: int, block: int, device="cpu") -> torch.Tensor:
-    """Queries of positions [64*block, 64*block+64): bf16 ``[B][Hq][64][D]``."""
-    shp = (wl.B, wl.Hq, BLOCK, wl.D)
-    return torch.randn(shp, generator=_gen(device, wl.seed, layer, _KIND_Q, block),
-                       device=device, dtype=torch.float32).to(torch.bfloat16)
+def kv_block(wl: Workload, layer: int, block: int, device="cpu", rows=None):
+    """Keys, values and eviction logits of positions [64*block, 64*block+64)
+    for batch rows ``rows`` (default: all; each row has its own stream).
+
+    Returns ``k, v``: bf16 ``[B'][Hkv][64][D]`` and ``logits``: float32
+    ``[B'][Hkv][64]``, on ``device``.
+    """
+    rows = range(wl.B) if rows is None else rows
+    parts = [_row_block_kv(wl, layer, block, int(b), device) for b in rows]
+    return (torch.stack([p[0] for p in parts]), torch.stack([p[1] for p in parts]),
+            torch.stack([p[2] for p in parts]))
+
+
+def q_block(wl: Workload, layer: int, block: int, device="cpu", rows=None) -> torch.Tensor:
+    """Queries of positions [64*block, 64*block+64): bf16 ``[B'][Hq][64][D]``."""
+    rows = range(wl.B) if rows is None else rows
+    return torch.stack([
+        torch.randn((wl.Hq, BLOCK, wl.D), generator=_gen(device, wl.seed, layer, _KIND_Q, block, int(b)),
+                    device=device, dtype=torch.float32).to(torch.bfloat16)
+        for b in rows])
 
 
 def kv_range(wl: Workload, layer: int, t0: int, t1: int, device="cpu", rows=None):
@@ -187,11 +199,9 @@ def kv_range(wl: Workload, layer: int, t0: int, t1: int, device="cpu", rows=None
     positions [t0, t1); ``rows`` selects batch rows (default: all)."""
     ks, vs, ls = [], [], []
     for blk in range(t0 // BLOCK, (t1 + BLOCK - 1) // BLOCK):
-        k, v, lg = kv_block(wl, layer, blk, device)
+        k, v, lg = kv_block(wl, layer, blk, device, rows)
         lo = max(t0, blk * BLOCK) - blk * BLOCK
         hi = min(t1, (blk + 1) * BLOCK) - blk * BLOCK
-        if rows is not None:
-            k, v, lg = k[rows], v[rows], lg[rows]
         ks.append(k[:, :, lo:hi])
         vs.append(v[:, :, lo:hi])
         ls.append(lg[:, :, lo:hi])
@@ -203,11 +213,9 @@ def q_range(wl: Workload, layer: int, t0: int, t1: int, device="cpu", rows=None)
     """Queries ``[B'][Hq][t1-t0][D]`` (bf16) of positions [t0, t1)."""
     qs = []
     for blk in range(t0 // BLOCK, (t1 + BLOCK - 1) // BLOCK):
-        q = q_block(wl, layer, blk, device)
+        q = q_block(wl, layer, blk, device, rows)
         lo = max(t0, blk * BLOCK) - blk * BLOCK
         hi = min(t1, (blk + 1) * BLOCK) - blk * BLOCK
-        if rows is not None:
-            q = q[rows]
         qs.append(q[:, :, lo:hi])
     return torch.cat(qs, 2).contiguous()
 
