@@ -1,0 +1,522 @@
+#!/usr/bin/env python
+"""Benchmark of the DMS decode hot path on B300.
+
+One step = one pass of the whole hot path for one token of every sequence:
+the fused append/evict kernel (decision, delayed eviction, slot reuse, K/V
+write), the split-K decode-attention kernel over the compacted caches and the
+kernel that merges the split heads' partial results.  Workload (default):
+Qwen3-8B-like attention -- batch 32, 32 query / 8 KV heads, head_dim 128,
+window 16, eviction logits N(1.150, 1) (CR 8) -- timed at context ~16K: the
+cache is filled to 16384 - W - 2K tokens with chunked appends, then W warm-up
+steps, K timed steps (pass A) and K steps with per-call events (pass B) end at
+16384.  The retained K/V (~270 MB) is larger than the 126 MB L2, so no flush
+is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Prints one JSON line on rank 0.  ``--impl reference`` times the CPU oracle on
+the host cores (the reference arm); under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn tokens/s and achieved HBM GB/s (% of peak) at CR 8, Qwen3-8B shapes"
+NOMINAL_HBM_GBS = 8000.0  # "roughly 8 TB/s" stated with the target
+FALLBACK_HBM_GBS = 6400.0
+PROFILE_FILE = os.path.join(ROOT, "profiles", "decode_kernel_qwen3-8b_cr8_n16384.md")
+KERNEL_SOURCES = ["decode.cuh", "dms_device.cuh"]
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "learned_kv_cache_eviction_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    try:
+        text = open(PROFILE_FILE).read()
+    except OSError:
+        return None
+    vals = {}
+    for ln in text.splitlines():
+        t = ln.strip().lstrip("-* ").strip()
+        if t.startswith(("traffic_bytes_per_launch", "kernel_source_sha256")) and ":" in t:
+            k, v = t.split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class _Nvml:
+    """Minimal read-only NVML access through ctypes (clock and clock-event
+    reason queries only; nothing is set)."""
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+
+    def handle(self, device_index: int):
+        ct = self.ct
+        h = ct.c_void_p()
+        try:
+            p = torch.cuda.get_device_properties(device_index)
+            pci = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0".encode()
+            if self.lib.nvmlDeviceGetHandleByPciBusId_v2(ct.c_char_p(pci), ct.byref(h)) == 0:
+                return h
+        except Exception:
+            pass
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ct.c_uint(device_index), ct.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        return h
+
+    def sm_clock(self, h) -> int:
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetClockInfo(h, 1, self.ct.byref(v))  # NVML_CLOCK_SM
+        return int(v.value)
+
+    def sm_max_clock(self, h) -> int:
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(h, 1, self.ct.byref(v))
+        return int(v.value)
+
+    def reasons(self, h) -> int:
+        v = self.ct.c_ulonglong()
+        self.lib.nvmlDeviceGetCurrentClocksEventReasons(h, self.ct.byref(v))
+        return int(v.value)
+
+
+class ClockSampler:
+    """Polls the SM clock and clock-event reasons through NVML during the timed
+    region (read-only)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
+
+    def __init__(self, device_index: int, period_s: float = 0.0005):
+        self.period = period_s
+        self.samples, self.reasons = [], set()
+        self._stop = threading.Event()
+        self.ok = False
+        self.err = ""
+        try:
+            self.nv = _Nvml()
+            self.h = self.nv.handle(device_index)
+            self.max_mhz = self.nv.sm_max_clock(self.h)
+            self.ok = True
+        except Exception as exc:  # no NVML: say so instead of clocks
+            self.err = repr(exc)[:200]
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.sm_clock(self.h))
+                r = self.nv.reasons(self.h)
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self.ok:
+            self.t.join()
+        return False
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": f"NVML unavailable: {self.err}"}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples), "source": "NVML (ctypes) polled every 0.5 ms during the timed steps"}
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+# ---------------------------------------------------------------------------
+# the native arm
+# ---------------------------------------------------------------------------
+
+def fill_cache(dms, W, wl, n0, device, layer=0):
+    cache = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w, device=device)
+    t = 0
+    while t < n0:
+        n = min(512, n0 - t)
+        k, v, lg = W.kv_range(wl, layer, t, t + n, device=device)
+        cache.append_chunk(k, v, lg)
+        t += n
+    torch.cuda.synchronize(device)
+    return cache
+
+
+def step_inputs(W, wl, t0, n, device, layer=0):
+    k, v, lg = W.kv_range(wl, layer, t0, t0 + n, device=device)
+    q = W.q_range(wl, layer, t0, t0 + n, device=device)
+    return ([q[:, :, i].contiguous() for i in range(n)], [k[:, :, i].contiguous() for i in range(n)],
+            [v[:, :, i].contiguous() for i in range(n)], [lg[:, :, i].contiguous() for i in range(n)])
+
+
+def time_device_leg(dms, cache, ins, warmup, steps, scale, device, clocks=None, dist=None):
+    """Warm-up, then two passes of ``steps`` steps through the C ABI on
+    device-resident inputs.  Pass A (the headline) records events only around
+    the whole pass, so consecutive kernels keep their programmatic-launch
+    overlap.  Pass B records events around every dms_decode_attention call
+    (decode + combine kernels) for the per-kernel roofline; those events
+    serialise the launches, so its times are upper bounds."""
+    lib = dms.load_library()
+    h = cache.handle
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    qs, ks, vs, ls = ins
+    Hq = qs[0].shape[1]
+    out = torch.empty((cache.batch, Hq, cache.head_dim), dtype=torch.float32, device=device)
+    outp = out.data_ptr()
+
+    def append(i):
+        rc = lib.dms_append(h, ks[i].data_ptr(), vs[i].data_ptr(), ls[i].data_ptr(), sh)
+        if rc:
+            raise dms.DmsError(rc, "dms_append")
+
+    def decode(i):
+        rc = lib.dms_decode_attention(h, qs[i].data_ptr(), outp, scale, Hq, sh)
+        if rc:
+            raise dms.DmsError(rc, "dms_decode_attention")
+
+    for i in range(warmup):
+        append(i)
+        decode(i)
+    torch.cuda.synchronize(device)
+    len0 = int(cache.lengths().sum())
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    with (clocks if clocks is not None else _Null()):
+        t_start.record(stream)
+        for i in range(warmup, warmup + steps):
+            append(i)
+            decode(i)
+        t_stop.record(stream)
+        torch.cuda.synchronize(device)
+    if dist is not None:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_stop)
+    len1 = int(cache.lengths().sum())
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for j in range(steps):
+        i = warmup + steps + j
+        append(i)
+        ev[j][0].record(stream)
+        decode(i)
+        ev[j][1].record(stream)
+    torch.cuda.synchronize(device)
+    len2 = int(cache.lengths().sum())
+    dec = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    st = cache.status()
+    if st != dms.DMS_OK:
+        raise dms.DmsError(st, "device status after the timed steps")
+    return {"total_ms": total_ms, "decode_us": statistics.mean(dec), "decode_us_median": statistics.median(dec),
+            "len_sum_start": len0, "len_sum_end": len1, "len_sum_b": 0.5 * (len1 + len2)}
+
+
+def time_e2e_leg(dms, W, wl, n0, warmup, steps, device):
+    """Same steps through the Python API with the step's inputs in pinned host
+    memory: every step copies q/k/v/logits host->device, runs append + decode,
+    copies the output device->host and waits for it."""
+    cache = fill_cache(dms, W, wl, n0, device)
+    ins = step_inputs(W, wl, n0, warmup + steps, device)
+    host = [[x.cpu().pin_memory() for x in lst] for lst in ins]
+    q_d = torch.empty_like(ins[0][0])
+    k_d = torch.empty_like(ins[1][0])
+    v_d = torch.empty_like(ins[2][0])
+    l_d = torch.empty_like(ins[3][0])
+    out_d = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device=device)
+    out_h = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(device)
+
+    def step(i):
+        q_d.copy_(host[0][i], non_blocking=True)
+        k_d.copy_(host[1][i], non_blocking=True)
+        v_d.copy_(host[2][i], non_blocking=True)
+        l_d.copy_(host[3][i], non_blocking=True)
+        cache.append(k_d, v_d, l_d)
+        cache.decode_attention(q_d, out_d, wl.scale)
+        out_h.copy_(out_d, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(warmup, warmup + steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = t0.elapsed_time(t1)
+    h2d = sum(x.numel() * x.element_size() for x in (q_d, k_d, v_d, l_d))
+    d2h = out_h.numel() * out_h.element_size()
+    assert bool(torch.isfinite(out_h).all())
+    cache.close()
+    return ms, h2d, d2h
+
+
+def decode_bytes(wl, len_sum):
+    """Algorithmic bytes of one decode call: retained K and V (bf16), q (bf16),
+    out (fp32) and the lengths (int32)."""
+    return len_sum * 2 * wl.D * 2 + wl.B * wl.Hq * wl.D * (2 + 4) + wl.B * wl.Hkv * 4
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p.get("num_threads", 1) for p in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_timer(wl, n_ctx, rows):
+    """Draw the oracle's inputs on the CPU for batch rows ``rows`` up to context
+    n_ctx; return a function running the oracle's decode step at position t."""
+    import oracle.dms_oracle as O
+    from learned_kv_cache_eviction_b300 import workload as W
+
+    k, v, lg = W.kv_range(wl, 0, 0, n_ctx, rows=rows)
+    q = W.q_range(wl, 0, n_ctx - 256, n_ctx, rows=rows)
+    k_np, v_np = k.float().numpy(), v.float().numpy()
+    e = O.eviction_decisions(lg.numpy())
+    q_np = q.float().numpy()
+
+    def run(t):
+        return O.decode_attention(q_np[:, :, t - (n_ctx - 256)], k_np, v_np, e, t, wl.w, wl.scale)
+    return run
+
+
+def cpu_baseline(wl, n_ctx, seconds=12.0, rows=(0, 1)):
+    run = oracle_timer(wl, n_ctx, list(rows))
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        run(n_ctx - 1 - (steps % 256))
+        steps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": len(rows) * steps / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"oracle decode step (mask + dense softmax attention) for batch rows {list(rows)} of "
+                      f"{wl.B} at positions {n_ctx - min(steps, 256)}..{n_ctx - 1} ({steps} steps, {dt:.1f} s)"}
+
+
+def workload_config(wl, n_ctx):
+    return {"workload": f"{wl.name} decode at context {n_ctx}: batch {wl.B}, {wl.Hq} query / {wl.Hkv} KV heads, "
+                        f"head_dim {wl.D}, window {wl.w}, eviction logits {wl.logits}",
+            "batch": wl.B, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "window": wl.w,
+            "context": n_ctx, "l2": "inputs larger than L2 (retained K/V > 126 MB), no flush"}
+
+
+def run_reference(args, wl):
+    rows = [0, 1]
+    n_ctx = wl.cap
+    run = oracle_timer(wl, n_ctx, rows)
+    for i in range(args.warmup):
+        run(n_ctx - 1 - (i % 256))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        run(n_ctx - 1 - (i % 256))
+    dt = time.perf_counter() - t0
+    value = len(rows) * args.steps / dt
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": workload_config(wl, n_ctx),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"each step: the oracle's decode step (mask + dense softmax attention) for "
+                                   f"batch rows {rows} of {wl.B} at a position in {n_ctx - 256}..{n_ctx - 1}"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="qwen3-8b")
+    ap.add_argument("--no-cr1", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from learned_kv_cache_eviction_b300 import workload as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = W.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, wl)
+        return
+
+    from learned_kv_cache_eviction_b300 import dms
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        dist = tdist
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    # weak scaling: every rank serves its own batch of independent sequences
+    wl_rank = wl.with_(seed=wl.seed + 1000 * rank) if rank else wl
+    n_end = wl.cap
+    n0 = n_end - args.warmup - 2 * args.steps  # warm-up, pass A (timed), pass B (per-call events)
+    if n0 < 1:
+        ap.error("warmup + 2 * steps must be below the capacity")
+
+    cache = fill_cache(dms, W, wl_rank, n0, device)
+    ins = step_inputs(W, wl_rank, n0, args.warmup + 2 * args.steps, device)
+    clocks = ClockSampler(device.index)
+    r = time_device_leg(dms, cache, ins, args.warmup, args.steps, wl.scale, device, clocks, dist)
+    cache.close()
+    del ins
+    total_ms = r["total_ms"]
+    if dist is not None:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    cr1 = None
+    if not args.no_cr1:
+        wl1 = W.WORKLOADS["qwen3-8b-cr1"] if args.workload == "qwen3-8b" else wl_rank.with_(logits=("const", -10.0))
+        if rank:
+            wl1 = wl1.with_(seed=wl1.seed + 1000 * rank)
+        c1 = fill_cache(dms, W, wl1, n0, device)
+        ins1 = step_inputs(W, wl1, n0, args.warmup + 2 * args.steps, device)
+        cr1 = time_device_leg(dms, c1, ins1, args.warmup, args.steps, wl.scale, device, None, dist)
+        c1.close()
+        del ins1
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = time_e2e_leg(dms, W, wl_rank, n0, args.warmup, args.steps, device)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    len_avg = 0.5 * (r["len_sum_start"] + r["len_sum_end"])
+    alg = decode_bytes(wl, r["len_sum_b"])
+    achieved = alg / (r["decode_us"] * 1e-6) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    value = wl.B * args.steps * world / (total_ms * 1e-3)
+    ctx_avg = n_end - 1.5 * args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage": "bf16 K/V/q, fp32 logits/out",
+        "data": "synthetic", "impl": "native",
+        "config": workload_config(wl, n_end),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} HBM copy bandwidth", "traffic": profiled_traffic(),
+                     "kernel": "dms_decode_attention call: decode_kernel + combine_kernel",
+                     "algorithmic_bytes_per_launch": alg, "us_per_launch": r["decode_us"],
+                     "frac_of_nominal_8TBps": achieved / NOMINAL_HBM_GBS},
+        "decode_attention": {"us_per_call_mean": r["decode_us"], "us_per_call_median": r["decode_us_median"],
+                             "note": "per-call events (decode + combine kernels, launch not overlapped)",
+                             "tokens_per_s": wl.B / (r["decode_us"] * 1e-6),
+                             "kv_token_reads_per_step": len_avg,
+                             "realised_cr": wl.B * wl.Hkv * ctx_avg / len_avg},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if cr1 is not None:
+        line["cr1"] = {"decode_us_per_call": cr1["decode_us"], "ms_per_step": cr1["total_ms"] / args.steps,
+                       "tokens_per_s": wl.B * args.steps / (cr1["total_ms"] * 1e-3),
+                       "achieved_GBps": decode_bytes(wl, cr1["len_sum_b"]) / (cr1["decode_us"] * 1e-6) / 1e9,
+                       "kv_token_reads_per_step": cr1["len_sum_b"],
+                       "decode_speedup_cr8_over_cr1": cr1["decode_us"] / r["decode_us"],
+                       "step_speedup_cr8_over_cr1": cr1["total_ms"] / r["total_ms"],
+                       "realised_cr": cr1["len_sum_b"] / r["len_sum_b"]}
+    if e2e is not None:
+        ms, h2d, d2h = e2e
+        line["e2e"] = {"value": wl.B * args.steps * world / (ms * 1e-3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "note": "Python API, pinned host inputs copied in and output copied out every step, "
+                               "stream synchronized every step"}
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, n_end)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

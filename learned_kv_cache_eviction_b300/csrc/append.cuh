@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(256) append_kernel(CacheView c, const uint4* _
                                                      const uint4* __restrict__ v,
                                                      const float* __restrict__ logit, int64_t t) {
   constexpr int CH = D / 8;
+  griddep_wait();
+  griddep_launch_dependents();
   const int i = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (i >= c.NH) return;
@@ -80,6 +82,8 @@ __global__ void __launch_bounds__(128) append_chunk_kernel(CacheView c, const ui
                                                            int chunk) {
   constexpr int CH = D / 8;
   __shared__ int slots_smem[4][32];
+  griddep_wait();
+  griddep_launch_dependents();
   const int wl = threadIdx.x >> 5;
   const int i = static_cast<int>(blockIdx.x * 4 + wl);
   const int lane = threadIdx.x & 31;

@@ -11,20 +11,20 @@
 //
 // Work split ("balanced by retained length"): the concatenation of all heads'
 // retained slots, S = sum(len) slots, is cut into Pe equal contiguous ranges,
-// one per warp of a persistent grid (one CTA per SM).  Each warp is an
-// independent flash-decoding worker:
-//   * lane 0 streams its range in tiles of TK slots (K tile and V tile, each
-//     one contiguous bulk copy global -> shared, completing on an mbarrier),
-//     NST tiles in flight;
-//   * QK: lane r computes the G scores of slot r of the tile over the full
-//     head dim (K rows are chunk-permuted in the pool, so these reads are free
-//     of bank conflicts while q is read as a broadcast);
-//   * online softmax in fp32, base-2 (q is pre-scaled by scale * log2 e);
-//   * PV: lane owns D/32 output elements of all G heads.
+// one per warp of a persistent grid (one CTA of up to 8 warps per SM).  Each
+// warp is an independent flash-decoding worker:
+//   * lane 0 streams its range in tiles of TK = 16 slots (K tile and V tile,
+//     each one contiguous bulk copy global -> shared completing on an
+//     mbarrier), NST = 3 tiles per warp in flight;
+//   * QK: lanes r and r + 16 score slot r of the tile over one half of the
+//     head dim each (K rows are chunk-permuted in the pool, so these reads are
+//     free of bank conflicts while q is read as a broadcast), then add;
+//   * online softmax in fp32, base 2 (q is pre-scaled by scale * log2 e);
+//   * PV: lane owns D/32 output elements of all G heads; packed fp32 FMAs.
 // A head covered by one warp is written directly.  A head split across
-// warps leaves one partial (max, sum, unnormalised acc) per warp; the warp
-// that finishes such a head last (an atomic arrival counter per head, no
-// waiting) merges the partials and resets the counter.
+// warps leaves one partial (max, sum, unnormalised acc) per warp, merged by
+// the combine kernel that follows in the stream (launched as a programmatic
+// dependent, so its launch overlaps the decode kernel).
 #pragma once
 
 #include "dms_device.cuh"
@@ -35,26 +35,37 @@ template <int D_, int G_>
 struct DecodeShape {
   static constexpr int D = D_;
   static constexpr int G = G_;
-  static constexpr int NW = 4;    // warps per CTA (one CTA per SM)
-  static constexpr int TK = 32;   // slots per tile
-  static constexpr int NST = 3;   // tiles in flight per warp
-  static constexpr int CH = D / 8;
-  static constexpr int EL = D / 32;  // output elements per lane
+  static constexpr int TK = 16;      // slots per tile
+  static constexpr int NST = 3;      // tiles in flight per warp
+  static constexpr int CH = D / 8;   // 16-byte chunks per K/V row
+  static constexpr int HCH = CH / 2; // chunks per half row (two lanes score one slot)
+  static constexpr int EL = D / 32;  // output elements per lane in PV
   static constexpr int ROWB = D * 2;
   static constexpr int TILEB = TK * ROWB;
-  static constexpr int GP = (G + 3) / 4 * 4;
+  // qs: fp32 q, per head g two half rows of D/2 floats, padded by 4 floats so
+  // that the two lane halves read different banks.
+  static constexpr int QHALF = D / 2 + 4;
+  static constexpr int QROW = 2 * QHALF;
+  // p buffer: per slot, the G probabilities as (p, p) pairs (operands of the
+  // packed fp32 FMA), padded to a multiple of 4 floats.
+  static constexpr int PROW = (2 * G + 3) / 4 * 4;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = NST * TILEB;
   static constexpr int OFF_QRAW = 2 * NST * TILEB;
   static constexpr int OFF_QS = OFF_QRAW + ((G * D * 2 + 127) / 128) * 128;
-  static constexpr int OFF_P = OFF_QS + G * D * 4;
-  static constexpr int OFF_BAR = OFF_P + TK * GP * 4;
+  static constexpr int OFF_P = OFF_QS + ((G * QROW * 4 + 15) / 16) * 16;
+  static constexpr int OFF_BAR = OFF_P + TK * PROW * 4;
   static constexpr int WARP_BYTES = ((OFF_BAR + (NST + 1) * 8 + 127) / 128) * 128;
+  static constexpr int kSmemBudget = 227 * 1024 - 1024;  // leaves room for static shared memory
+  static constexpr int NW = (kSmemBudget / WARP_BYTES) < 8 ? (kSmemBudget / WARP_BYTES) : 8;
   static constexpr int SMEM = NW * WARP_BYTES;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(G >= 1 && G <= 8, "1 <= G <= 8");
-  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(NW >= 4, "at least four warps per CTA");
 };
+
+// Largest number of warps per CTA of any instantiation (sizes the partials).
+constexpr int kMaxWarpsPerCta = 8;
 
 // Fewest retained slots a warp is given (bounds the number of partials when
 // the cache is small).
@@ -68,7 +79,7 @@ struct DecodeArgs {
   float* out;         // fp32 [B][Hq][D]
   float* part_acc;    // [entries][G][D]
   float* part_ml;     // [entries][G][2]
-  int32_t* head_cnt;  // [NH], zero between launches
+  int32_t* pre_out;   // [NH + 1] prefix sums of len, written by CTA 0 for the combine kernel
   int32_t* err;
   int NH, Hkv, cap;
   float qscale;  // scale * log2(e)
@@ -152,17 +163,89 @@ __device__ __forceinline__ void scan_lengths(const int32_t* __restrict__ len, in
   __syncthreads();
 }
 
+// Merge the nseg partials (max m, sum l, unnormalised acc) of one head, stored
+// at consecutive partial indices base, base + 1, ..., and write the normalised
+// output (outp already offset by lane * EL).  Loads for all G heads are issued
+// together: one pass for (max, sum), one for the accumulators.
+template <int D, int G>
+__device__ __forceinline__ void merge_partials(const DecodeArgs& a, size_t base, int nseg, float* outp, int lane) {
+  constexpr int EL = D / 32;
+  const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
+  float M[G], L[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    M[g] = -INFINITY;
+    L[g] = 0.f;
+  }
+  for (int k = lane; k < nseg; k += 32) {
+    float2 v[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) v[g] = __ldcg(ml + (base + k) * G + g);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float mn = fmaxf(M[g], v[g].x);
+      L[g] = L[g] * fast_exp2(M[g] - mn) + v[g].y * fast_exp2(v[g].x - mn);
+      M[g] = mn;
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float Mo = __shfl_xor_sync(0xffffffffu, M[g], off);
+      const float Lo = __shfl_xor_sync(0xffffffffu, L[g], off);
+      const float mn = fmaxf(M[g], Mo);
+      if (mn != -INFINITY) {
+        L[g] = L[g] * fast_exp2(M[g] - mn) + Lo * fast_exp2(Mo - mn);
+        M[g] = mn;
+      }
+    }
+  }
+  float2 acc[G][EL / 2];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int e = 0; e < EL / 2; ++e) acc[g][e] = make_float2(0.f, 0.f);
+  }
+#pragma unroll 2
+  for (int k = 0; k < nseg; ++k) {
+    const size_t kk = base + k;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float wk = fast_exp2(__ldcg(ml + kk * G + g).x - M[g]);
+      const float2* src = reinterpret_cast<const float2*>(a.part_acc + (kk * G + g) * D + lane * EL);
+#pragma unroll
+      for (int e = 0; e < EL / 2; ++e) acc[g][e] = __ffma2_rn(make_float2(wk, wk), __ldcg(src + e), acc[g][e]);
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float inv = 1.f / L[g];
+#pragma unroll
+    for (int e = 0; e < EL / 2; ++e)
+      reinterpret_cast<float2*>(outp + g * D)[e] = make_float2(acc[g][e].x * inv, acc[g][e].y * inv);
+  }
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(const DecodeArgs a) {
   using Sh = DecodeShape<D, G>;
-  constexpr int NW = Sh::NW, TK = Sh::TK, NST = Sh::NST, CH = Sh::CH, EL = Sh::EL;
-  constexpr int GP = Sh::GP, ROWB = Sh::ROWB, TILEB = Sh::TILEB;
+  constexpr int NW = Sh::NW, TK = Sh::TK, NST = Sh::NST, CH = Sh::CH, HCH = Sh::HCH, EL = Sh::EL;
+  constexpr int ROWB = Sh::ROWB, TILEB = Sh::TILEB, QHALF = Sh::QHALF, QROW = Sh::QROW, PROW = Sh::PROW;
   extern __shared__ __align__(1024) uint8_t smem[];
+
+  // Launched as a programmatic dependent of the previous kernel: everything the
+  // previous kernels wrote is visible after this wait.
+  griddep_wait();
+  griddep_launch_dependents();
 
   // ---- prologue: prefix sums of the retained lengths, warp ranges ----
   int* pre = reinterpret_cast<int*>(smem);  // aliases the warp regions until the barrier below
   scan_lengths(a.len, a.NH, pre);
   const int64_t S = pre[a.NH];
+  if (blockIdx.x == 0) {
+    for (int x = threadIdx.x; x <= a.NH; x += blockDim.x) a.pre_out[x] = pre[x];
+  }
   const int wl = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int64_t Pe = static_cast<int64_t>(gridDim.x) * NW;
   if (S / kMinSlotsPerWarp < Pe) Pe = S / kMinSlotsPerWarp;
@@ -238,6 +321,8 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
     if (nq_issued > nq_conv) (void)mbar_wait(qbar, nq_conv & 1);
   };
 
+  // QK lane roles: two lanes per slot, each over half of the head dim.
+  const int r = lane & 15, hf = lane >> 4;
   float m[G], l[G];
   float2 o[G][EL / 2];
   int seg_i = 0, seg_L = 0;
@@ -255,8 +340,9 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
 #pragma unroll
       for (int x = lane; x < G * D / 2; x += 32) {
         const float2 f = bf16x2_to_float2(qw[x]);
-        qs[2 * x] = f.x * a.qscale;
-        qs[2 * x + 1] = f.y * a.qscale;
+        const int g = (2 * x) / D, d = (2 * x) % D;
+        const int dst = g * QROW + (d >= D / 2 ? QHALF + d - D / 2 : d);
+        *reinterpret_cast<float2*>(qs + dst) = make_float2(f.x * a.qscale, f.y * a.qscale);
       }
       __syncwarp();
       ++nq_conv;
@@ -281,27 +367,27 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
       return;
     }
 
-    // ---- QK: lane r scores slot s0 + r for all G heads ----
+    // ---- QK: lanes r and r + 16 score slot s0 + r over the two halves of D ----
     float sc[G];
     {
-      const uint4* Kt = reinterpret_cast<const uint4*>(Ks + buf * TILEB);
-      if (lane < cnt) {
-        const int sw = (s0 + lane) & 7;
-        const uint4* krow = Kt + lane * CH;
-        float2 acc0[G], acc1[G];
+      const uint4* krow = reinterpret_cast<const uint4*>(Ks + buf * TILEB) + r * CH;
+      const int sw = (s0 + r) & 7;
+      const float* qh = qs + hf * QHALF;
+      float2 acc0[G], acc1[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          acc0[g] = make_float2(0.f, 0.f);
-          acc1[g] = make_float2(0.f, 0.f);
-        }
+      for (int g = 0; g < G; ++g) {
+        acc0[g] = make_float2(0.f, 0.f);
+        acc1[g] = make_float2(0.f, 0.f);
+      }
+      if (r < cnt) {
 #pragma unroll
-        for (int c = 0; c < CH; ++c) {
-          const uint4 kk = krow[c ^ sw];
+        for (int c = 0; c < HCH; ++c) {
+          const uint4 kk = krow[(hf * HCH + c) ^ sw];
           const float2 k0 = bf16x2_to_float2(kk.x), k1 = bf16x2_to_float2(kk.y);
           const float2 k2 = bf16x2_to_float2(kk.z), k3 = bf16x2_to_float2(kk.w);
 #pragma unroll
           for (int g = 0; g < G; ++g) {
-            const float4* qp = reinterpret_cast<const float4*>(qs + g * D + c * 8);
+            const float4* qp = reinterpret_cast<const float4*>(qh + g * QROW + c * 8);
             const float4 qa = qp[0], qb = qp[1];
             acc0[g] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc0[g]);
             acc1[g] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc1[g]);
@@ -309,28 +395,35 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
             acc1[g] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc1[g]);
           }
         }
+      }
 #pragma unroll
-        for (int g = 0; g < G; ++g) sc[g] = (acc0[g].x + acc0[g].y) + (acc1[g].x + acc1[g].y);
-      } else {
-#pragma unroll
-        for (int g = 0; g < G; ++g) sc[g] = -INFINITY;
+      for (int g = 0; g < G; ++g) {
+        float sg = (acc0[g].x + acc0[g].y) + (acc1[g].x + acc1[g].y);
+        sg += __shfl_xor_sync(0xffffffffu, sg, 16);
+        sc[g] = r < cnt ? sg : -INFINITY;
       }
     }
 
-    // ---- online softmax (base 2) ----
+    // ---- online softmax (base 2); lanes r and r + 16 hold the same scores ----
     {
       bool rescale = false;
-      float alpha[G];
+      float alpha[G], p[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float mt = warp_max(sc[g]);
+        float mt = sc[g];
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
         const float mn = fmaxf(m[g], mt);
         alpha[g] = fast_exp2(m[g] - mn);
-        const float p = fast_exp2(sc[g] - mn);
-        l[g] = l[g] * alpha[g] + p;
+        p[g] = fast_exp2(sc[g] - mn);
+        l[g] = l[g] * alpha[g] + (hf == 0 ? p[g] : 0.f);
         m[g] = mn;
-        pb[lane * GP + g] = p;
         rescale |= alpha[g] != 1.f;
+      }
+      if (hf == 0) {
+        float2* prow = reinterpret_cast<float2*>(pb + r * PROW);
+#pragma unroll
+        for (int g = 0; g < G; ++g) prow[g] = make_float2(p[g], p[g]);
       }
       if (rescale) {
 #pragma unroll
@@ -355,24 +448,21 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
         } else {
           v2[0] = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(Vt + j * ROWB));
         }
-        float pj[GP];
+        const float4* prow = reinterpret_cast<const float4*>(pb + j * PROW);
 #pragma unroll
-        for (int x = 0; x < GP / 4; ++x) {
-          const float4 p4 = *reinterpret_cast<const float4*>(pb + j * GP + 4 * x);
-          pj[4 * x + 0] = p4.x;
-          pj[4 * x + 1] = p4.y;
-          pj[4 * x + 2] = p4.z;
-          pj[4 * x + 3] = p4.w;
-        }
+        for (int x = 0; x < (G + 1) / 2; ++x) {
+          const float4 p4 = prow[x];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float2 pp = make_float2(pj[g], pj[g]);
+          for (int e = 0; e < EL / 2; ++e) o[2 * x][e] = __ffma2_rn(make_float2(p4.x, p4.y), v2[e], o[2 * x][e]);
+          if (2 * x + 1 < G) {
 #pragma unroll
-          for (int e = 0; e < EL / 2; ++e) o[g][e] = __ffma2_rn(pp, v2[e], o[g][e]);
+            for (int e = 0; e < EL / 2; ++e)
+              o[2 * x + 1][e] = __ffma2_rn(make_float2(p4.z, p4.w), v2[e], o[2 * x + 1][e]);
+          }
         }
       };
       if (cnt == TK) {
-#pragma unroll 8
+#pragma unroll
         for (int j = 0; j < TK; ++j) pv_row(j);
       } else {
         for (int j = 0; j < cnt; ++j) pv_row(j);
@@ -385,21 +475,20 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
     const bool seg_end = !cs.valid || cs.i != cur_i;
 
     if (seg_end) {
-      // ---- segment end: direct output, or partial + last-arriver merge ----
+      // ---- segment end: direct output, or a partial for the combine kernel ----
 #pragma unroll
       for (int g = 0; g < G; ++g) l[g] = warp_sum(l[g]);
       const int b = seg_i / a.Hkv, h = seg_i - b * a.Hkv;
-      float* outp = a.out + (static_cast<size_t>(b) * Hq + h * G) * D + lane * EL;
       const int64_t w0 = ((seg_P + 1) * Pe - 1) / S;
       const int64_t w1 = ((seg_P + seg_L) * Pe - 1) / S;
       if (w0 == w1) {
+        float* outp = a.out + (static_cast<size_t>(b) * Hq + h * G) * D + lane * EL;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float inv = 1.f / l[g];
 #pragma unroll
-          for (int e = 0; e < EL / 2; ++e) {
+          for (int e = 0; e < EL / 2; ++e)
             reinterpret_cast<float2*>(outp + g * D)[e] = make_float2(o[g][e].x * inv, o[g][e].y * inv);
-          }
         }
       } else {
         const size_t idx = static_cast<size_t>(wg + seg_i);
@@ -418,50 +507,38 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
               ll = l[g];
             }
           }
-          reinterpret_cast<float2*>(a.part_ml + idx * G * 2)[lane] = make_float2(mm, ll);
-        }
-        __threadfence();
-        __syncwarp();
-        int old = 0;
-        if (lane == 0) old = atomicAdd(&a.head_cnt[seg_i], 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == static_cast<int>(w1 - w0)) {
-          __threadfence();
-          for (int g = 0; g < G; ++g) {
-            float M = -INFINITY;
-            for (int64_t k = w0 + lane; k <= w1; k += 32) {
-              M = fmaxf(M, __ldcg(a.part_ml + (static_cast<size_t>(k + seg_i) * G + g) * 2));
-            }
-            M = warp_max(M);
-            float Ls = 0.f;
-            for (int64_t k = w0 + lane; k <= w1; k += 32) {
-              const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml) +
-                                       static_cast<size_t>(k + seg_i) * G + g);
-              Ls += ml.y * fast_exp2(ml.x - M);
-            }
-            Ls = warp_sum(Ls);
-            float2 acc[EL / 2];
-#pragma unroll
-            for (int e = 0; e < EL / 2; ++e) acc[e] = make_float2(0.f, 0.f);
-            for (int64_t k = w0; k <= w1; ++k) {
-              const size_t kk = static_cast<size_t>(k + seg_i);
-              const float wk = fast_exp2(__ldcg(a.part_ml + (kk * G + g) * 2) - M);
-              const float2* src = reinterpret_cast<const float2*>(a.part_acc + (kk * G + g) * D + lane * EL);
-#pragma unroll
-              for (int e = 0; e < EL / 2; ++e) acc[e] = __ffma2_rn(make_float2(wk, wk), __ldcg(src + e), acc[e]);
-            }
-            const float inv = 1.f / Ls;
-#pragma unroll
-            for (int e = 0; e < EL / 2; ++e) {
-              reinterpret_cast<float2*>(outp + g * D)[e] = make_float2(acc[e].x * inv, acc[e].y * inv);
-            }
-          }
-          if (lane == 0) a.head_cnt[seg_i] = 0;
+          reinterpret_cast<float2*>(a.part_ml)[idx * G + lane] = make_float2(mm, ll);
         }
       }
     }
     try_issue();
   }
+}
+
+// Merge the partials of every head that the decode kernel split across warps
+// (one warp per head; heads covered by one warp were written directly).
+// decode_warps: the decode launch's grid size x warps per CTA.
+template <int D, int G>
+__global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, int decode_warps) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int i = static_cast<int>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (i >= a.NH) return;
+  const int64_t S = a.pre_out[a.NH];
+  int64_t Pe = decode_warps;
+  if (S / kMinSlotsPerWarp < Pe) Pe = S / kMinSlotsPerWarp;
+  if (Pe < 1) Pe = 1;
+  const int64_t P = a.pre_out[i];
+  const int64_t L = a.pre_out[i + 1] - P;
+  if (L <= 0) return;
+  const int64_t w0 = ((P + 1) * Pe - 1) / S;
+  const int64_t w1 = ((P + L) * Pe - 1) / S;
+  if (w0 == w1) return;
+  const int Hq = a.Hkv * G;
+  const int b = i / a.Hkv, h = i - b * a.Hkv;
+  float* outp = a.out + (static_cast<size_t>(b) * Hq + h * G) * D + lane * (D / 32);
+  merge_partials<D, G>(a, static_cast<size_t>(w0 + i), static_cast<int>(w1 - w0) + 1, outp, lane);
 }
 
 }  // namespace dms

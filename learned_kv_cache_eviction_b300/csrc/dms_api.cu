@@ -10,6 +10,7 @@
 #include <mutex>
 #include <new>
 #include <unordered_set>
+#include <utility>
 
 #include "append.cuh"
 #include "decode.cuh"
@@ -23,7 +24,7 @@ struct dms_cache {
   dms::CacheView view;
   float* part_acc;
   float* part_ml;
-  int32_t* head_cnt;
+  int32_t* pre;  // [NH + 1] prefix sums of len (decode -> combine)
   size_t part_entries;
 };
 
@@ -72,6 +73,29 @@ bool device_pointer_ok(const void* p, int dev) {
 
 int launch_status() { return cudaGetLastError() == cudaSuccess ? DMS_OK : DMS_ERR_CUDA; }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel in the stream is still running; every kernel of
+// this library calls griddepcontrol.wait before touching global memory, so
+// stream order is preserved for data while launch latency is overlapped.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return DMS_ERR_CUDA;
+  }
+  return launch_status();
+}
+
 template <int D, int G>
 int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaStream_t st) {
   using Sh = dms::DecodeShape<D, G>;
@@ -96,14 +120,16 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
   a.out = out;
   a.part_acc = c->part_acc;
   a.part_ml = c->part_ml;
-  a.head_cnt = c->head_cnt;
+  a.pre_out = c->pre;
   a.err = c->view.err;
   a.NH = c->NH;
   a.Hkv = c->H;
   a.cap = c->cap;
   a.qscale = scale * 1.4426950408889634f;  // log2(e): softmax evaluated as 2^(x log2 e)
-  dms::decode_kernel<D, G><<<grid, Sh::NW * 32, Sh::SMEM, st>>>(a);
-  return launch_status();
+  int rc = launch_pdl(dms::decode_kernel<D, G>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
+  if (rc != DMS_OK) return rc;
+  const int decode_warps = grid * Sh::NW;
+  return launch_pdl(dms::combine_kernel<D, G>, dim3((c->NH + 7) / 8), dim3(256), 0, st, a, decode_warps);
 }
 
 template <int D>
@@ -131,7 +157,7 @@ void free_cache_memory(dms_cache* c) {
   cudaFree(c->view.err);
   cudaFree(c->part_acc);
   cudaFree(c->part_ml);
-  cudaFree(c->head_cnt);
+  cudaFree(c->pre);
 }
 
 }  // namespace
@@ -188,8 +214,7 @@ dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_di
   const size_t pool = static_cast<size_t>(NH) * capacity * head_dim * 2;
   const size_t nslot = static_cast<size_t>(NH) * capacity;
   const size_t nring = static_cast<size_t>(NH) * window;
-  constexpr int kNWMax = 4;  // warps per CTA of the decode kernel
-  c->part_entries = static_cast<size_t>(c->num_sms) * kNWMax + NH;
+  c->part_entries = static_cast<size_t>(c->num_sms) * dms::kMaxWarpsPerCta + NH;
   const size_t part_acc = c->part_entries * DMS_MAX_GROUP * head_dim * sizeof(float);
   const size_t part_ml = c->part_entries * DMS_MAX_GROUP * 2 * sizeof(float);
   bool ok = cudaMalloc(&c->view.K, pool) == cudaSuccess && cudaMalloc(&c->view.V, pool) == cudaSuccess &&
@@ -198,12 +223,12 @@ dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_di
             cudaMalloc(&c->view.ring_flag, nring) == cudaSuccess &&
             cudaMalloc(&c->view.len, NH * 4) == cudaSuccess && cudaMalloc(&c->view.err, kAlign) == cudaSuccess &&
             cudaMalloc(&c->part_acc, part_acc) == cudaSuccess && cudaMalloc(&c->part_ml, part_ml) == cudaSuccess &&
-            cudaMalloc(&c->head_cnt, NH * 4) == cudaSuccess;
+            cudaMalloc(&c->pre, (NH + 1) * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->view.K, 0, pool) == cudaSuccess && cudaMemset(c->view.V, 0, pool) == cudaSuccess &&
        cudaMemset(c->view.slot_pos, 0xff, nslot * 4) == cudaSuccess &&
        cudaMemset(c->view.ring_slot, 0xff, nring * 4) == cudaSuccess &&
        cudaMemset(c->view.ring_flag, 0, nring) == cudaSuccess && cudaMemset(c->view.len, 0, NH * 4) == cudaSuccess &&
-       cudaMemset(c->view.err, 0, kAlign) == cudaSuccess && cudaMemset(c->head_cnt, 0, NH * 4) == cudaSuccess &&
+       cudaMemset(c->view.err, 0, kAlign) == cudaSuccess && cudaMemset(c->pre, 0, (NH + 1) * 4) == cudaSuccess &&
        cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
@@ -248,13 +273,13 @@ int dms_append(dms_cache_t* c, const void* k, const void* v, const float* evict_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int threads = 256;
   const int blocks = (c->NH * 32 + threads - 1) / threads;
-  if (c->D == 128)
-    dms::append_kernel<128><<<blocks, threads, 0, st>>>(c->view, static_cast<const uint4*>(k),
-                                                        static_cast<const uint4*>(v), evict_logit, c->t);
-  else
-    dms::append_kernel<64><<<blocks, threads, 0, st>>>(c->view, static_cast<const uint4*>(k),
-                                                       static_cast<const uint4*>(v), evict_logit, c->t);
-  const int rc = launch_status();
+  const uint4* k4 = static_cast<const uint4*>(k);
+  const uint4* v4 = static_cast<const uint4*>(v);
+  const int rc = c->D == 128
+                     ? launch_pdl(dms::append_kernel<128>, dim3(blocks), dim3(threads), 0, st, c->view, k4, v4,
+                                  evict_logit, c->t)
+                     : launch_pdl(dms::append_kernel<64>, dim3(blocks), dim3(threads), 0, st, c->view, k4, v4,
+                                  evict_logit, c->t);
   if (rc == DMS_OK) c->t += 1;
   return rc;
 }
@@ -269,13 +294,12 @@ int dms_append_chunk(dms_cache_t* c, const void* k, const void* v, const float* 
     return DMS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int blocks = (c->NH + 3) / 4;
-  if (c->D == 128)
-    dms::append_chunk_kernel<128><<<blocks, 128, 0, st>>>(c->view, static_cast<const uint4*>(k),
-                                                          static_cast<const uint4*>(v), logits, c->t, chunk);
-  else
-    dms::append_chunk_kernel<64><<<blocks, 128, 0, st>>>(c->view, static_cast<const uint4*>(k),
-                                                         static_cast<const uint4*>(v), logits, c->t, chunk);
-  const int rc = launch_status();
+  const uint4* k4 = static_cast<const uint4*>(k);
+  const uint4* v4 = static_cast<const uint4*>(v);
+  const int rc = c->D == 128 ? launch_pdl(dms::append_chunk_kernel<128>, dim3(blocks), dim3(128), 0, st, c->view,
+                                          k4, v4, logits, c->t, chunk)
+                             : launch_pdl(dms::append_chunk_kernel<64>, dim3(blocks), dim3(128), 0, st, c->view,
+                                          k4, v4, logits, c->t, chunk);
   if (rc == DMS_OK) c->t += chunk;
   return rc;
 }

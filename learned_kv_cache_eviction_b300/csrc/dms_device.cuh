@@ -86,6 +86,15 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their writes are visible; allow the next grid in the stream to
+// be scheduled (it still waits for this grid's completion before its own wait
+// returns).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 2^x (PTX ex2.approx, flush-to-zero; ex2(-inf) = +0).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
