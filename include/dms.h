@@ -40,6 +40,7 @@ extern "C" {
 #define DMS_ERR_BAD_HANDLE (-4)  /* NULL, destroyed or foreign cache handle */
 #define DMS_ERR_TIMEOUT (-5)     /* sticky: a device-side wait passed its time limit */
 #define DMS_ERR_EMPTY (-6)       /* decode before any token was appended */
+#define DMS_ERR_SCRATCH_LIMIT (-7) /* problem too large for the fixed scratch of dms_decode_attention_noalloc */
 
 /* Largest query-head group per KV head (Hq / Hkv) the decode kernel supports. */
 #define DMS_MAX_GROUP 8
@@ -129,6 +130,50 @@ int64_t dms_cache_position(dms_cache_t* cache);
 
 /* Static description of a code. */
 const char* dms_error_string(int code);
+
+/*
+ * Decode attention without any device allocation.  (The paper has no
+ * counterpart: this entry point exists for callers, not for the method.)
+ *
+ * Some callers cannot call cudaMalloc when they decode: an inference engine
+ * that reserved all device memory for its own pool at start-up, code running
+ * where the caching allocator must not grow, or a component that is only
+ * handed pointers to buffers another component owns.  This call computes the
+ * same result as dms_decode_attention, but reads the cache from caller-owned
+ * buffers and keeps the decode kernels' split-K scratch in a fixed array of
+ * DMS_NOALLOC_SCRATCH_BYTES that the library holds in device memory on every
+ * GPU that loads it, until the process exits.  It calls no allocating routine.
+ *
+ *   k_pool, v_pool  bf16 [batch][kv_heads][capacity][head_dim], the retained
+ *                   tokens of (b, h) in slots [0, len[b][h]).  V rows are in
+ *                   plain element order.  K rows use the library's layout:
+ *                   16-byte chunk c of slot s is stored at chunk c ^ (s & 7).
+ *   len             int32 [batch][kv_heads], each >= 1 (device memory)
+ *   q, out, scale, q_heads: as for dms_decode_attention.
+ * All pointers are device memory of the current device, 16-byte aligned
+ * (len 4-byte aligned).
+ *
+ * Limits: batch * kv_heads <= DMS_NOALLOC_MAX_HEADS, and the scratch a call
+ * needs, about (8 * SM count + batch * kv_heads) * G * (head_dim + 2) * 4
+ * bytes plus 4 bytes per head (G = q_heads / kv_heads), must fit in
+ * DMS_NOALLOC_SCRATCH_BYTES; otherwise DMS_ERR_SCRATCH_LIMIT is returned and
+ * nothing is enqueued.  (On a 148-SM B300 with head_dim 128 that allows about
+ * 2000 heads at G = 4 and about 800 at G = 8.)
+ *
+ * The first call on a device looks up the scratch array's device address and
+ * zeroes its error word (a synchronous step), so make that first call before
+ * any stream capture.  Every call shares the one array: calls whose kernels
+ * overlap on the GPU (other streams, other host threads) race on it and must
+ * be ordered by the caller.  Nothing in the array needs to start at zero
+ * between calls -- each call writes every scratch value it reads.  A device
+ * wait that times out is latched in the array's error word; this call does not
+ * report it.
+ */
+#define DMS_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define DMS_NOALLOC_MAX_HEADS 2048
+int dms_decode_attention_noalloc(const void* k_pool, const void* v_pool, const int32_t* len, int batch,
+                                 int kv_heads, int capacity, int head_dim, const void* q, float* out,
+                                 float scale, int q_heads, void* stream);
 
 #ifdef __cplusplus
 }

@@ -13,7 +13,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG_DIR, "libdms.so")
-SOURCES = ["dms_api.cu"]
+SOURCES = ["dms_api.cu", "noalloc.cu"]
 HEADERS = ["append.cuh", "decode.cuh", "dms_device.cuh"]
 
 NVCC_FLAGS = [

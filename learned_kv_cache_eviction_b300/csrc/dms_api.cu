@@ -175,6 +175,7 @@ const char* dms_error_string(int code) {
     case DMS_ERR_BAD_HANDLE: return "bad cache handle";
     case DMS_ERR_TIMEOUT: return "device wait timed out (sticky)";
     case DMS_ERR_EMPTY: return "cache is empty";
+    case DMS_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed scratch of the no-allocation entry point";
     default: return "unknown error";
   }
 }

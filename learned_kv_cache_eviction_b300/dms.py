@@ -22,6 +22,7 @@ DMS_ERR_CAPACITY = -3
 DMS_ERR_BAD_HANDLE = -4
 DMS_ERR_TIMEOUT = -5
 DMS_ERR_EMPTY = -6
+DMS_ERR_SCRATCH_LIMIT = -7
 DMS_MAX_GROUP = 8
 
 # Entry points declared in include/dms.h: name -> (restype, argtypes)
@@ -40,6 +41,7 @@ SIGNATURES = {
     "dms_cache_status": (_I, [_P, _P]),
     "dms_cache_position": (ctypes.c_int64, [_P]),
     "dms_error_string": (ctypes.c_char_p, [_I]),
+    "dms_decode_attention_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, ctypes.c_float, _I, _P]),
 }
 
 _lib = None
