@@ -103,8 +103,10 @@ int dms_append_chunk(dms_cache_t* cache, const void* k, const void* v, const flo
  * q_heads must be a multiple of kv_heads with q_heads / kv_heads <= 8.
  * The retained slots of all heads are split evenly across the warps of a
  * persistent grid (flash-decoding split-K balanced by retained length); the
- * partial results of a head split across warps are merged on the device by
- * the last warp to finish it.  Returns DMS_ERR_EMPTY if nothing was appended.
+ * partial results of a head split across warps are merged by a second kernel
+ * enqueued right after it on the same stream.  Uses the split-K scratch that
+ * dms_cache_create allocated; allocates nothing.  Returns DMS_ERR_EMPTY if
+ * nothing was appended.
  */
 int dms_decode_attention(dms_cache_t* cache, const void* q, float* out, float scale, int q_heads,
                          void* stream);
@@ -154,18 +156,19 @@ const char* dms_error_string(int code);
  * (len 4-byte aligned).
  *
  * Limits: batch * kv_heads <= DMS_NOALLOC_MAX_HEADS, and the scratch a call
- * needs, about (8 * SM count + batch * kv_heads) * G * (head_dim + 2) * 4
+ * needs, about (12 * SM count + batch * kv_heads) * G * (head_dim + 2) * 4
  * bytes plus 4 bytes per head (G = q_heads / kv_heads), must fit in
  * DMS_NOALLOC_SCRATCH_BYTES; otherwise DMS_ERR_SCRATCH_LIMIT is returned and
- * nothing is enqueued.  (On a 148-SM B300 with head_dim 128 that allows about
- * 2000 heads at G = 4 and about 800 at G = 8.)
+ * nothing is enqueued.  (On a 148-SM B300 with head_dim 128 that allows the
+ * full 2048 heads at G = 4 and about 800 at G = 8.)
  *
  * The first call on a device looks up the scratch array's device address and
  * zeroes its error word (a synchronous step), so make that first call before
  * any stream capture.  Every call shares the one array: calls whose kernels
  * overlap on the GPU (other streams, other host threads) race on it and must
- * be ordered by the caller.  Nothing in the array needs to start at zero
- * between calls -- each call writes every scratch value it reads.  A device
+ * be ordered by the caller.  Each call first clears the per-head counters it
+ * uses (a stream-ordered memset, which allocates nothing) and writes every
+ * other scratch value before reading it.  A device
  * wait that times out is latched in the array's error word; this call does not
  * report it.
  */

@@ -11,20 +11,24 @@
 //
 // Work split ("balanced by retained length"): the concatenation of all heads'
 // retained slots, S = sum(len) slots, is cut into Pe equal contiguous ranges,
-// one per warp of a persistent grid (one CTA of up to 8 warps per SM).  Each
-// warp is an independent flash-decoding worker:
+// one per warp of a persistent grid (one CTA of up to 12 warps per SM, so that
+// each of the SM's four schedulers gets the same number of warps).  Each warp is
+// an independent flash-decoding worker:
 //   * lane 0 streams its range in tiles of TK = 16 slots (K tile and V tile,
 //     each one contiguous bulk copy global -> shared completing on an
-//     mbarrier), NST = 3 tiles per warp in flight;
+//     mbarrier), NST = 2 tiles per warp in flight; when a tile opens a new
+//     head, the lanes also load that head's G query rows into registers, to be
+//     widened into shared memory when the head's first tile is consumed;
 //   * QK: lanes r and r + 16 score slot r of the tile over one half of the
 //     head dim each (K rows are chunk-permuted in the pool, so these reads are
 //     free of bank conflicts while q is read as a broadcast), then add;
 //   * online softmax in fp32, base 2 (q is pre-scaled by scale * log2 e);
 //   * PV: lane owns D/32 output elements of all G heads; packed fp32 FMAs.
-// A head covered by one warp is written directly.  A head split across
-// warps leaves one partial (max, sum, unnormalised acc) per warp, merged by
-// the combine kernel that follows in the stream (launched as a programmatic
-// dependent, so its launch overlaps the decode kernel).
+// A head covered by one warp is normalised and written directly.  A head split
+// across warps leaves one partial (max, sum, unnormalised acc) per warp; each
+// such warp then increments the head's arrival counter, and the warp that
+// arrives last merges the partials and writes the output (and resets the
+// counter for the next call).  No warp ever waits for another.
 #pragma once
 
 #include "dms_device.cuh"
@@ -36,7 +40,7 @@ struct DecodeShape {
   static constexpr int D = D_;
   static constexpr int G = G_;
   static constexpr int TK = 16;      // slots per tile
-  static constexpr int NST = 3;      // tiles in flight per warp
+  static constexpr int NST = 2;      // tiles in flight per warp
   static constexpr int CH = D / 8;   // 16-byte chunks per K/V row
   static constexpr int HCH = CH / 2; // chunks per half row (two lanes score one slot)
   static constexpr int EL = D / 32;  // output elements per lane in PV
@@ -51,13 +55,17 @@ struct DecodeShape {
   static constexpr int PROW = (2 * G + 3) / 4 * 4;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = NST * TILEB;
-  static constexpr int OFF_QRAW = 2 * NST * TILEB;
-  static constexpr int OFF_QS = OFF_QRAW + ((G * D * 2 + 127) / 128) * 128;
+  static constexpr int OFF_QS = 2 * NST * TILEB;
+  static constexpr int QV = (G * D / 8 + 31) / 32;  // 16-byte q chunks per lane
   static constexpr int OFF_P = OFF_QS + ((G * QROW * 4 + 15) / 16) * 16;
   static constexpr int OFF_BAR = OFF_P + TK * PROW * 4;
-  static constexpr int WARP_BYTES = ((OFF_BAR + (NST + 1) * 8 + 127) / 128) * 128;
+  static constexpr int WARP_BYTES = ((OFF_BAR + NST * 8 + 127) / 128) * 128;
   static constexpr int kSmemBudget = 227 * 1024 - 1024;  // leaves room for static shared memory
-  static constexpr int NW = (kSmemBudget / WARP_BYTES) < 8 ? (kSmemBudget / WARP_BYTES) : 8;
+  // Warps per CTA: 12 (three per scheduler) where the shared memory allows.  With
+  // three warps on a scheduler its register file leaves 168 registers per thread;
+  // G >= 7 needs more, so those shapes run two warps per scheduler.
+  static constexpr int NW_CAP = G >= 7 ? 8 : 12;
+  static constexpr int NW = (kSmemBudget / WARP_BYTES) < NW_CAP ? (kSmemBudget / WARP_BYTES) : NW_CAP;
   static constexpr int SMEM = NW * WARP_BYTES;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(G >= 1 && G <= 8, "1 <= G <= 8");
@@ -65,7 +73,7 @@ struct DecodeShape {
 };
 
 // Largest number of warps per CTA of any instantiation (sizes the partials).
-constexpr int kMaxWarpsPerCta = 8;
+constexpr int kMaxWarpsPerCta = 12;
 
 // Fewest retained slots a warp is given (bounds the number of partials when
 // the cache is small).
@@ -79,7 +87,7 @@ struct DecodeArgs {
   float* out;         // fp32 [B][Hq][D]
   float* part_acc;    // [entries][G][D]
   float* part_ml;     // [entries][G][2]
-  int32_t* pre_out;   // [NH + 1] prefix sums of len, written by CTA 0 for the combine kernel
+  int32_t* head_cnt;  // [NH] arrival counters of split heads; zero between calls
   int32_t* err;
   int NH, Hkv, cap;
   float qscale;  // scale * log2(e)
@@ -127,14 +135,17 @@ struct TileIter {
   }
 };
 
-// Exclusive scan of len[0..NH) into pre[0..NH] by the whole CTA.
+// Exclusive prefix sums of len[0..NH) into pre[0..NH] (shared memory) by the
+// whole CTA, reading each length from global memory once.
 __device__ __forceinline__ void scan_lengths(const int32_t* __restrict__ len, int NH, int* pre) {
   __shared__ int wsum[32];
   const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  for (int x = tid; x < NH; x += nt) pre[x] = len[x];
+  __syncthreads();
   const int per = (NH + nt - 1) / nt;
   const int b0 = min(NH, tid * per), b1 = min(NH, b0 + per);
   int sum = 0;
-  for (int x = b0; x < b1; ++x) sum += len[x];
+  for (int x = b0; x < b1; ++x) sum += pre[x];
   int incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -154,10 +165,12 @@ __device__ __forceinline__ void scan_lengths(const int32_t* __restrict__ len, in
     wsum[lane] = inc - v;
   }
   __syncthreads();
+  // Each thread rewrites only its own range [b0, b1), which no other thread reads.
   int run = wsum[wid] + incl - sum;
   for (int x = b0; x < b1; ++x) {
+    const int l = pre[x];
     pre[x] = run;
-    run += len[x];
+    run += l;
   }
   if (tid == nt - 1) pre[NH] = run;
   __syncthreads();
@@ -165,8 +178,11 @@ __device__ __forceinline__ void scan_lengths(const int32_t* __restrict__ len, in
 
 // Merge the nseg partials (max m, sum l, unnormalised acc) of one head, stored
 // at consecutive partial indices base, base + 1, ..., and write the normalised
-// output (outp already offset by lane * EL).  Loads for all G heads are issued
-// together: one pass for (max, sum), one for the accumulators.
+// output (outp already offset by lane * EL).  Partials written by other SMs are
+// read from L2 (ld.global.cg).  Pass 1 reduces (max, sum) with the segments
+// spread over the lanes; pass 2 takes 32 segments at a time, each lane
+// computing one segment's weight, broadcast by shuffles while the
+// accumulators' loads of several segments are in flight together.
 template <int D, int G>
 __device__ __forceinline__ void merge_partials(const DecodeArgs& a, size_t base, int nseg, float* outp, int lane) {
   constexpr int EL = D / 32;
@@ -207,15 +223,22 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, size_t base,
 #pragma unroll
     for (int e = 0; e < EL / 2; ++e) acc[g][e] = make_float2(0.f, 0.f);
   }
-#pragma unroll 2
-  for (int k = 0; k < nseg; ++k) {
-    const size_t kk = base + k;
+  for (int kb = 0; kb < nseg; kb += 32) {
+    float wv[G];
+    const int k = kb + lane;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float wk = fast_exp2(__ldcg(ml + kk * G + g).x - M[g]);
-      const float2* src = reinterpret_cast<const float2*>(a.part_acc + (kk * G + g) * D + lane * EL);
+    for (int g = 0; g < G; ++g) wv[g] = k < nseg ? fast_exp2(__ldcg(ml + (base + k) * G + g).x - M[g]) : 0.f;
+    const int n = min(32, nseg - kb);
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) {
+      const size_t kk = base + kb + j;
 #pragma unroll
-      for (int e = 0; e < EL / 2; ++e) acc[g][e] = __ffma2_rn(make_float2(wk, wk), __ldcg(src + e), acc[g][e]);
+      for (int g = 0; g < G; ++g) {
+        const float wk = __shfl_sync(0xffffffffu, wv[g], j);
+        const float2* src = reinterpret_cast<const float2*>(a.part_acc + (kk * G + g) * D + lane * EL);
+#pragma unroll
+        for (int e = 0; e < EL / 2; ++e) acc[g][e] = __ffma2_rn(make_float2(wk, wk), __ldcg(src + e), acc[g][e]);
+      }
     }
   }
 #pragma unroll
@@ -243,9 +266,6 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
   int* pre = reinterpret_cast<int*>(smem);  // aliases the warp regions until the barrier below
   scan_lengths(a.len, a.NH, pre);
   const int64_t S = pre[a.NH];
-  if (blockIdx.x == 0) {
-    for (int x = threadIdx.x; x <= a.NH; x += blockDim.x) a.pre_out[x] = pre[x];
-  }
   const int wl = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int64_t Pe = static_cast<int64_t>(gridDim.x) * NW;
   if (S / kMinSlotsPerWarp < Pe) Pe = S / kMinSlotsPerWarp;
@@ -272,13 +292,11 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
   uint8_t* wbase = smem + wl * Sh::WARP_BYTES;
   uint8_t* Ks = wbase + Sh::OFF_K;
   uint8_t* Vs = wbase + Sh::OFF_V;
-  uint8_t* qraw = wbase + Sh::OFF_QRAW;
   float* qs = reinterpret_cast<float*>(wbase + Sh::OFF_QS);
   float* pb = reinterpret_cast<float*>(wbase + Sh::OFF_P);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + Sh::OFF_BAR);  // [NST] tiles, [NST] = q
-  uint64_t* qbar = bars + NST;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + Sh::OFF_BAR);  // [NST] tiles
   if (lane == 0) {
-    for (int x = 0; x <= NST; ++x) mbar_init(&bars[x], 1);
+    for (int x = 0; x < NST; ++x) mbar_init(&bars[x], 1);
     fence_barrier_init();
   }
   __syncwarp();
@@ -288,9 +306,12 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
   is.start(a.len, i0, P0, A, E);
   cs = is;
   int n_issued = 0, n_cons = 0, nq_issued = 0, nq_conv = 0;
+  constexpr int QV = Sh::QV;
+  uint4 qpre[QV];  // bf16 q rows of the next segment, 8 elements per chunk
 
   // Issue tiles ahead while buffers are free.  A segment's first tile also
-  // brings that segment's q; the single q buffer must have been consumed.
+  // starts the load of that segment's q into qpre, which must have been
+  // consumed by the previous segment.
   auto try_issue = [&]() {
     while (is.valid && n_issued < n_cons + NST) {
       if (is.first && nq_issued != nq_conv) break;
@@ -302,13 +323,17 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
         mbar_arrive_expect_tx(&bars[buf], 2 * bytes);
         bulk_copy_g2s(Ks + buf * TILEB, a.K + row * CH, bytes, &bars[buf]);
         bulk_copy_g2s(Vs + buf * TILEB, a.V + row * CH, bytes, &bars[buf]);
-        if (is.first) {
-          const int b = is.i / a.Hkv, h = is.i - (is.i / a.Hkv) * a.Hkv;
-          mbar_arrive_expect_tx(qbar, G * D * 2);
-          bulk_copy_g2s(qraw, a.q + (static_cast<size_t>(b) * Hq + h * G) * D, G * D * 2, qbar);
-        }
       }
-      if (is.first) ++nq_issued;
+      if (is.first) {
+        const int b = is.i / a.Hkv, h = is.i - (is.i / a.Hkv) * a.Hkv;
+        const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * Hq + h * G) * D);
+#pragma unroll
+        for (int v = 0; v < QV; ++v) {
+          const int x = lane + 32 * v;
+          if (x < G * D / 8) qpre[v] = __ldg(qsrc + x);
+        }
+        ++nq_issued;
+      }
       ++n_issued;
       is.advance(a.len, a.NH, cnt);
     }
@@ -318,7 +343,6 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
   auto fail_and_drain = [&]() {
     if (lane == 0) atomicOr(a.err, kErrBitTimeout);
     for (int k = n_cons; k < n_issued; ++k) (void)mbar_wait(&bars[k % NST], (k / NST) & 1);
-    if (nq_issued > nq_conv) (void)mbar_wait(qbar, nq_conv & 1);
   };
 
   // QK lane roles: two lanes per slot, each over half of the head dim.
@@ -332,17 +356,20 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
   while (cs.valid) {
     if (cs.first) {
       // ---- segment start: this head's q (bf16) -> qs (fp32, pre-scaled) ----
-      if (nq_issued <= nq_conv || !mbar_wait(qbar, nq_conv & 1)) {
-        fail_and_drain();
-        return;
-      }
-      const uint32_t* qw = reinterpret_cast<const uint32_t*>(qraw);
+      // (the first tile of this segment was issued, so its q is in qpre)
 #pragma unroll
-      for (int x = lane; x < G * D / 2; x += 32) {
-        const float2 f = bf16x2_to_float2(qw[x]);
-        const int g = (2 * x) / D, d = (2 * x) % D;
-        const int dst = g * QROW + (d >= D / 2 ? QHALF + d - D / 2 : d);
-        *reinterpret_cast<float2*>(qs + dst) = make_float2(f.x * a.qscale, f.y * a.qscale);
+      for (int v = 0; v < QV; ++v) {
+        const int x = lane + 32 * v;
+        if (x < G * D / 8) {
+          const int e0 = 8 * x, g = e0 / D, d = e0 % D;
+          float* dst = qs + g * QROW + (d >= D / 2 ? QHALF + d - D / 2 : d);
+          const uint4 u = qpre[v];
+          const float2 f0 = bf16x2_to_float2(u.x), f1 = bf16x2_to_float2(u.y);
+          const float2 f2 = bf16x2_to_float2(u.z), f3 = bf16x2_to_float2(u.w);
+          const float sc = a.qscale;
+          reinterpret_cast<float4*>(dst)[0] = make_float4(f0.x * sc, f0.y * sc, f1.x * sc, f1.y * sc);
+          reinterpret_cast<float4*>(dst)[1] = make_float4(f2.x * sc, f2.y * sc, f3.x * sc, f3.y * sc);
+        }
       }
       __syncwarp();
       ++nq_conv;
@@ -475,14 +502,15 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
     const bool seg_end = !cs.valid || cs.i != cur_i;
 
     if (seg_end) {
-      // ---- segment end: direct output, or a partial for the combine kernel ----
+      // ---- segment end: direct output, or a partial merged by the last arriver ----
 #pragma unroll
       for (int g = 0; g < G; ++g) l[g] = warp_sum(l[g]);
       const int b = seg_i / a.Hkv, h = seg_i - b * a.Hkv;
+      float* outp = a.out + (static_cast<size_t>(b) * Hq + h * G) * D + lane * EL;
+      // Warps holding the first and the last slot of this head.
       const int64_t w0 = ((seg_P + 1) * Pe - 1) / S;
       const int64_t w1 = ((seg_P + seg_L) * Pe - 1) / S;
       if (w0 == w1) {
-        float* outp = a.out + (static_cast<size_t>(b) * Hq + h * G) * D + lane * EL;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float inv = 1.f / l[g];
@@ -491,6 +519,8 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
             reinterpret_cast<float2*>(outp + g * D)[e] = make_float2(o[g][e].x * inv, o[g][e].y * inv);
         }
       } else {
+        // Partial of (warp wg, head seg_i) at index wg + seg_i: unique, because the
+        // heads a warp covers never decrease with the warp index.
         const size_t idx = static_cast<size_t>(wg + seg_i);
         float* pa = a.part_acc + idx * G * D + lane * EL;
 #pragma unroll
@@ -509,36 +539,23 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
           }
           reinterpret_cast<float2*>(a.part_ml)[idx * G + lane] = make_float2(mm, ll);
         }
+        // Release the partial, then count this arrival; the last of the head's
+        // nseg warps merges (acquire) and resets the counter.
+        const int nseg = static_cast<int>(w1 - w0) + 1;
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(a.head_cnt + seg_i, 1) == nseg - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          merge_partials<D, G>(a, static_cast<size_t>(w0 + seg_i), nseg, outp, lane);
+          if (lane == 0) a.head_cnt[seg_i] = 0;
+        }
       }
     }
     try_issue();
   }
-}
-
-// Merge the partials of every head that the decode kernel split across warps
-// (one warp per head; heads covered by one warp were written directly).
-// decode_warps: the decode launch's grid size x warps per CTA.
-template <int D, int G>
-__global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, int decode_warps) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const int i = static_cast<int>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (i >= a.NH) return;
-  const int64_t S = a.pre_out[a.NH];
-  int64_t Pe = decode_warps;
-  if (S / kMinSlotsPerWarp < Pe) Pe = S / kMinSlotsPerWarp;
-  if (Pe < 1) Pe = 1;
-  const int64_t P = a.pre_out[i];
-  const int64_t L = a.pre_out[i + 1] - P;
-  if (L <= 0) return;
-  const int64_t w0 = ((P + 1) * Pe - 1) / S;
-  const int64_t w1 = ((P + L) * Pe - 1) / S;
-  if (w0 == w1) return;
-  const int Hq = a.Hkv * G;
-  const int b = i / a.Hkv, h = i - b * a.Hkv;
-  float* outp = a.out + (static_cast<size_t>(b) * Hq + h * G) * D + lane * (D / 32);
-  merge_partials<D, G>(a, static_cast<size_t>(w0 + i), static_cast<int>(w1 - w0) + 1, outp, lane);
 }
 
 }  // namespace dms

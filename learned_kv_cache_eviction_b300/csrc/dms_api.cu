@@ -24,7 +24,7 @@ struct dms_cache {
   dms::CacheView view;
   float* part_acc;
   float* part_ml;
-  int32_t* pre;  // [NH + 1] prefix sums of len (decode -> combine)
+  int32_t* head_cnt;  // [NH] arrival counters of heads split across warps (zero between calls)
   size_t part_entries;
 };
 
@@ -120,16 +120,13 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
   a.out = out;
   a.part_acc = c->part_acc;
   a.part_ml = c->part_ml;
-  a.pre_out = c->pre;
+  a.head_cnt = c->head_cnt;
   a.err = c->view.err;
   a.NH = c->NH;
   a.Hkv = c->H;
   a.cap = c->cap;
   a.qscale = scale * 1.4426950408889634f;  // log2(e): softmax evaluated as 2^(x log2 e)
-  int rc = launch_pdl(dms::decode_kernel<D, G>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
-  if (rc != DMS_OK) return rc;
-  const int decode_warps = grid * Sh::NW;
-  return launch_pdl(dms::combine_kernel<D, G>, dim3((c->NH + 7) / 8), dim3(256), 0, st, a, decode_warps);
+  return launch_pdl(dms::decode_kernel<D, G>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
 }
 
 template <int D>
@@ -157,7 +154,7 @@ void free_cache_memory(dms_cache* c) {
   cudaFree(c->view.err);
   cudaFree(c->part_acc);
   cudaFree(c->part_ml);
-  cudaFree(c->pre);
+  cudaFree(c->head_cnt);
 }
 
 }  // namespace
@@ -224,12 +221,12 @@ dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_di
             cudaMalloc(&c->view.ring_flag, nring) == cudaSuccess &&
             cudaMalloc(&c->view.len, NH * 4) == cudaSuccess && cudaMalloc(&c->view.err, kAlign) == cudaSuccess &&
             cudaMalloc(&c->part_acc, part_acc) == cudaSuccess && cudaMalloc(&c->part_ml, part_ml) == cudaSuccess &&
-            cudaMalloc(&c->pre, (NH + 1) * 4) == cudaSuccess;
+            cudaMalloc(&c->head_cnt, NH * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->view.K, 0, pool) == cudaSuccess && cudaMemset(c->view.V, 0, pool) == cudaSuccess &&
        cudaMemset(c->view.slot_pos, 0xff, nslot * 4) == cudaSuccess &&
        cudaMemset(c->view.ring_slot, 0xff, nring * 4) == cudaSuccess &&
        cudaMemset(c->view.ring_flag, 0, nring) == cudaSuccess && cudaMemset(c->view.len, 0, NH * 4) == cudaSuccess &&
-       cudaMemset(c->view.err, 0, kAlign) == cudaSuccess && cudaMemset(c->pre, 0, (NH + 1) * 4) == cudaSuccess &&
+       cudaMemset(c->view.err, 0, kAlign) == cudaSuccess && cudaMemset(c->head_cnt, 0, NH * 4) == cudaSuccess &&
        cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     cudaGetLastError();

@@ -25,8 +25,8 @@
 
 namespace {
 
-// Split-K scratch of one call: partial (acc, max, sum) per (warp, head) segment,
-// the prefix sums of the lengths, and the device error word.  8 MiB.
+// Split-K scratch of one call: the device error word, one arrival counter per
+// head, and the partial (acc, max, sum) of every (warp, head) segment.  8 MiB.
 constexpr size_t kScratchBytes = DMS_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
@@ -97,12 +97,13 @@ int run(int dev, int num_sms, unsigned char* scratch, const void* k_pool, const 
   const int64_t smax = static_cast<int64_t>(NH) * capacity;
   const int64_t per_cta = int64_t(dms::kMinSlotsPerWarp) * Sh::NW;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms, (smax + per_cta - 1) / per_cta)));
-  // Scratch layout: [0, 256) error word; partial acc; partial (max, sum); prefix sums.
+  // Scratch layout: [0, 256) error word; head counters; partial acc; partial (max, sum).
   const size_t entries = static_cast<size_t>(grid) * Sh::NW + NH;
+  const size_t cnt_off = 256;
+  const size_t acc_off = cnt_off + ((static_cast<size_t>(NH) * 4 + 255) / 256) * 256;
   const size_t acc_bytes = entries * G * D * sizeof(float);
   const size_t ml_bytes = entries * G * 2 * sizeof(float);
-  const size_t pre_off = 256 + ((acc_bytes + ml_bytes + 255) / 256) * 256;
-  if (pre_off + static_cast<size_t>(NH + 1) * 4 > kScratchBytes) return DMS_ERR_SCRATCH_LIMIT;
+  if (acc_off + acc_bytes + ml_bytes > kScratchBytes) return DMS_ERR_SCRATCH_LIMIT;
   if (dev < kMaxDevices && !g_attr_done[dev][D == 128][G]) {
     if (cudaFuncSetAttribute(dms::decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) !=
         cudaSuccess) {
@@ -118,16 +119,21 @@ int run(int dev, int num_sms, unsigned char* scratch, const void* k_pool, const 
   a.q = static_cast<const uint16_t*>(q);
   a.out = out;
   a.err = reinterpret_cast<int32_t*>(scratch);
-  a.part_acc = reinterpret_cast<float*>(scratch + 256);
-  a.part_ml = reinterpret_cast<float*>(scratch + 256 + acc_bytes);
-  a.pre_out = reinterpret_cast<int32_t*>(scratch + pre_off);
+  a.head_cnt = reinterpret_cast<int32_t*>(scratch + cnt_off);
+  a.part_acc = reinterpret_cast<float*>(scratch + acc_off);
+  a.part_ml = reinterpret_cast<float*>(scratch + acc_off + acc_bytes);
   a.NH = NH;
   a.Hkv = kv_heads;
   a.cap = capacity;
   a.qscale = scale * 1.4426950408889634f;  // log2(e)
-  int rc = launch_dependent(dms::decode_kernel<D, G>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
-  if (rc != DMS_OK) return rc;
-  return launch_dependent(dms::combine_kernel<D, G>, dim3((NH + 7) / 8), dim3(256), 0, st, a, grid * Sh::NW);
+  // The merge in the decode kernel needs every head counter at zero.  Calls that
+  // complete leave them at zero; clearing them here (stream-ordered, no
+  // allocation) also recovers from a call that stopped early.
+  if (cudaMemsetAsync(a.head_cnt, 0, static_cast<size_t>(NH) * 4, st) != cudaSuccess) {
+    cudaGetLastError();
+    return DMS_ERR_CUDA;
+  }
+  return launch_dependent(dms::decode_kernel<D, G>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
 }
 
 template <int D>
