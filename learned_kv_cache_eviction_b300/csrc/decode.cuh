@@ -63,8 +63,8 @@ struct DecodeShape {
   static constexpr int kSmemBudget = 227 * 1024 - 1024;  // leaves room for static shared memory
   // Warps per CTA: 12 (three per scheduler) where the shared memory allows.  With
   // three warps on a scheduler its register file leaves 168 registers per thread;
-  // G >= 7 needs more, so those shapes run two warps per scheduler.
-  static constexpr int NW_CAP = G >= 7 ? 8 : 12;
+  // G >= 5 needs more, so those shapes run two warps per scheduler.
+  static constexpr int NW_CAP = G >= 5 ? 8 : 12;
   static constexpr int NW = (kSmemBudget / WARP_BYTES) < NW_CAP ? (kSmemBudget / WARP_BYTES) : NW_CAP;
   static constexpr int SMEM = NW * WARP_BYTES;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
@@ -180,9 +180,10 @@ __device__ __forceinline__ void scan_lengths(const int32_t* __restrict__ len, in
 // at consecutive partial indices base, base + 1, ..., and write the normalised
 // output (outp already offset by lane * EL).  Partials written by other SMs are
 // read from L2 (ld.global.cg).  Pass 1 reduces (max, sum) with the segments
-// spread over the lanes; pass 2 takes 32 segments at a time, each lane
-// computing one segment's weight, broadcast by shuffles while the
-// accumulators' loads of several segments are in flight together.
+// spread over the lanes, each lane keeping its first segment's values; pass 2
+// takes 32 segments at a time, each lane computing one segment's weight,
+// broadcast by shuffles while the accumulators' loads of several segments are
+// in flight together.
 template <int D, int G>
 __device__ __forceinline__ void merge_partials(const DecodeArgs& a, size_t base, int nseg, float* outp, int lane) {
   constexpr int EL = D / 32;
@@ -193,10 +194,15 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, size_t base,
     M[g] = -INFINITY;
     L[g] = 0.f;
   }
+  float2 v0[G];  // this lane's segment among the first 32, kept for pass 2
   for (int k = lane; k < nseg; k += 32) {
     float2 v[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) v[g] = __ldcg(ml + (base + k) * G + g);
+    if (k == lane) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) v0[g] = v[g];
+    }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const float mn = fmaxf(M[g], v[g].x);
@@ -227,7 +233,10 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, size_t base,
     float wv[G];
     const int k = kb + lane;
 #pragma unroll
-    for (int g = 0; g < G; ++g) wv[g] = k < nseg ? fast_exp2(__ldcg(ml + (base + k) * G + g).x - M[g]) : 0.f;
+    for (int g = 0; g < G; ++g) {
+      const float mk = kb == 0 ? v0[g].x : (k < nseg ? __ldcg(ml + (base + k) * G + g).x : 0.f);
+      wv[g] = k < nseg ? fast_exp2(mk - M[g]) : 0.f;
+    }
     const int n = min(32, nseg - kb);
 #pragma unroll 4
     for (int j = 0; j < n; ++j) {
