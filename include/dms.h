@@ -94,6 +94,25 @@ int dms_append_chunk(dms_cache_t* cache, const void* k, const void* v, const flo
                      int chunk, void* stream);
 
 /*
+ * Chunked prefill: attention for `chunk` new tokens (positions t .. t+chunk-1,
+ * t = tokens appended so far), then their append.  The result equals `chunk`
+ * rounds of dms_append followed by dms_decode_attention, one per token:
+ *   q       bf16 [batch][q_heads][chunk][head_dim]
+ *   k, v    bf16 [batch][kv_heads][chunk][head_dim]
+ *   logits  fp32 [batch][kv_heads][chunk]        decision = (logit > 0)
+ *   out     fp32 [batch][q_heads][chunk][head_dim]
+ * The query of token c sees the retained cache and the chunk's tokens up to c
+ * under the delayed eviction of the method ("Inference-Time Hyper-Scaling with
+ * KV Cache Compression", AI research-map summary, "Approach"): a token marked
+ * for eviction stays visible for the w - 1 positions after its own.  The
+ * attention runs on the tensor cores (bf16 Q K^T, fp32 softmax, P V with p
+ * carried as two bf16 terms, fp32 accumulation); then the chunk is appended
+ * as by dms_append_chunk.  q_heads as for dms_decode_attention.
+ */
+int dms_prefill(dms_cache_t* cache, const void* q, const void* k, const void* v, const float* logits, int chunk,
+                float* out, float scale, int q_heads, void* stream);
+
+/*
  * Decode attention for the query of the last appended token, over every
  * retained slot of each (sequence, KV head):
  *   q    bf16 [batch][q_heads][head_dim]

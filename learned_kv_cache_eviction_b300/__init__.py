@@ -14,5 +14,6 @@ from .dms import (  # noqa: F401
     dms_cache_slot_positions,
     dms_cache_status,
     dms_decode_attention,
+    dms_prefill,
     load_library,
 )

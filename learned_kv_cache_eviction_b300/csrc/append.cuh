@@ -73,7 +73,9 @@ __global__ void __launch_bounds__(256) append_kernel(CacheView c, const uint4* _
 // `chunk` appends per (sequence, KV head) in position order, one warp per
 // head.  Lane 0 assigns the slots of up to 32 tokens at a time sequentially
 // (bit-identical to single appends, including chains where a token retires
-// another token of the same chunk); then the warp copies those rows.
+// another token of the same chunk); then the warp copies those rows, skipping
+// a row whose slot a later token of the same batch takes over (that token
+// retired it), so that no slot is written twice by one batch.
 // k, v: [NH][chunk][D/8] chunks; logits: [NH][chunk].
 template <int D>
 __global__ void __launch_bounds__(128) append_chunk_kernel(CacheView c, const uint4* __restrict__ k,
@@ -95,7 +97,11 @@ __global__ void __launch_bounds__(128) append_chunk_kernel(CacheView c, const ui
     if (lane == 0) {
       for (int j = 0; j < n; ++j) {
         const float lg = logits[static_cast<size_t>(i) * chunk + base + j];
-        slots[j] = append_bookkeeping(c, i, t0 + base + j, lg, len_reg);
+        const int s = append_bookkeeping(c, i, t0 + base + j, lg, len_reg);
+        slots[j] = s;
+        // Token j took the slot of token j - w (which it retired): if that token
+        // is in this batch, it is not copied, so the slot is written once.
+        if (s >= 0 && j >= c.w && slots[j - c.w] == s) slots[j - c.w] = -1;
       }
     }
     __syncwarp();

@@ -15,6 +15,7 @@
 #include "append.cuh"
 #include "decode.cuh"
 #include "dms.h"
+#include "prefill.cuh"
 
 struct dms_cache {
   int B, H, cap, D, w, NH;
@@ -142,6 +143,47 @@ int launch_decode_d(dms_cache* c, const void* q, float* out, float scale, int G,
     case 8: return launch_decode_t<D, 8>(c, q, out, scale, st);
     default: return DMS_ERR_INVALID_ARG;
   }
+}
+
+template <int D, int G>
+int launch_prefill_t(dms_cache* c, const dms::PrefillArgs& a, cudaStream_t st) {
+  using Sh = dms::PrefillShape<D, G>;
+  static bool attr_done[64] = {};
+  if (c->device < 64 && !attr_done[c->device]) {
+    if (cudaFuncSetAttribute(dms::prefill_attention_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Sh::SMEM) != cudaSuccess) {
+      cudaGetLastError();
+      return DMS_ERR_CUDA;
+    }
+    attr_done[c->device] = true;
+  }
+  const dim3 grid((a.C + Sh::PT - 1) / Sh::PT, c->NH);
+  return launch_pdl(dms::prefill_attention_kernel<D, G>, grid, dim3(128), Sh::SMEM, st, a);
+}
+
+template <int D>
+int launch_prefill_d(dms_cache* c, const dms::PrefillArgs& a, int G, cudaStream_t st) {
+  switch (G) {
+    case 1: return launch_prefill_t<D, 1>(c, a, st);
+    case 2: return launch_prefill_t<D, 2>(c, a, st);
+    case 3: return launch_prefill_t<D, 3>(c, a, st);
+    case 4: return launch_prefill_t<D, 4>(c, a, st);
+    case 5: return launch_prefill_t<D, 5>(c, a, st);
+    case 6: return launch_prefill_t<D, 6>(c, a, st);
+    case 7: return launch_prefill_t<D, 7>(c, a, st);
+    case 8: return launch_prefill_t<D, 8>(c, a, st);
+    default: return DMS_ERR_INVALID_ARG;
+  }
+}
+
+int launch_append_chunk(dms_cache* c, const void* k, const void* v, const float* logits, int chunk, cudaStream_t st) {
+  const int blocks = (c->NH + 3) / 4;
+  const uint4* k4 = static_cast<const uint4*>(k);
+  const uint4* v4 = static_cast<const uint4*>(v);
+  return c->D == 128 ? launch_pdl(dms::append_chunk_kernel<128>, dim3(blocks), dim3(128), 0, st, c->view, k4, v4,
+                                  logits, c->t, chunk)
+                     : launch_pdl(dms::append_chunk_kernel<64>, dim3(blocks), dim3(128), 0, st, c->view, k4, v4,
+                                  logits, c->t, chunk);
 }
 
 void free_cache_memory(dms_cache* c) {
@@ -290,14 +332,47 @@ int dms_append_chunk(dms_cache_t* c, const void* k, const void* v, const float* 
   if (!g.ok) return DMS_ERR_CUDA;
   if (!device_pointer_ok(k, c->device) || !device_pointer_ok(v, c->device) || !device_pointer_ok(logits, c->device))
     return DMS_ERR_INVALID_ARG;
+  const int rc = launch_append_chunk(c, k, v, logits, chunk, static_cast<cudaStream_t>(stream));
+  if (rc == DMS_OK) c->t += chunk;
+  return rc;
+}
+
+int dms_prefill(dms_cache_t* c, const void* q, const void* k, const void* v, const float* logits, int chunk,
+                float* out, float scale, int q_heads, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  if (chunk < 1 || !q || !k || !v || !logits || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      !aligned16(logits) || !aligned16(out) || q_heads < 1 || q_heads % c->H != 0 ||
+      q_heads / c->H > DMS_MAX_GROUP || !std::isfinite(scale) || c->t + chunk > INT32_MAX)
+    return DMS_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return DMS_ERR_CUDA;
+  if (!device_pointer_ok(q, c->device) || !device_pointer_ok(k, c->device) || !device_pointer_ok(v, c->device) ||
+      !device_pointer_ok(logits, c->device) || !device_pointer_ok(out, c->device))
+    return DMS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int blocks = (c->NH + 3) / 4;
-  const uint4* k4 = static_cast<const uint4*>(k);
-  const uint4* v4 = static_cast<const uint4*>(v);
-  const int rc = c->D == 128 ? launch_pdl(dms::append_chunk_kernel<128>, dim3(blocks), dim3(128), 0, st, c->view,
-                                          k4, v4, logits, c->t, chunk)
-                             : launch_pdl(dms::append_chunk_kernel<64>, dim3(blocks), dim3(128), 0, st, c->view,
-                                          k4, v4, logits, c->t, chunk);
+  dms::PrefillArgs a;
+  a.K = c->view.K;
+  a.V = c->view.V;
+  a.len = c->view.len;
+  a.slot_pos = c->view.slot_pos;
+  a.ring_flag = c->view.ring_flag;
+  a.q = static_cast<const uint4*>(q);
+  a.kc = static_cast<const uint4*>(k);
+  a.vc = static_cast<const uint4*>(v);
+  a.logits = logits;
+  a.out = out;
+  a.err = c->view.err;
+  a.NH = c->NH;
+  a.Hkv = c->H;
+  a.cap = c->cap;
+  a.w = c->w;
+  a.C = chunk;
+  a.t0 = static_cast<int>(c->t);
+  a.qscale = scale * 1.4426950408889634f;  // log2(e)
+  const int G = q_heads / c->H;
+  int rc = c->D == 128 ? launch_prefill_d<128>(c, a, G, st) : launch_prefill_d<64>(c, a, G, st);
+  if (rc != DMS_OK) return rc;
+  rc = launch_append_chunk(c, k, v, logits, chunk, st);
   if (rc == DMS_OK) c->t += chunk;
   return rc;
 }

@@ -35,6 +35,7 @@ SIGNATURES = {
     "dms_append": (_I, [_P, _P, _P, _P, _P]),
     "dms_append_chunk": (_I, [_P, _P, _P, _P, _I, _P]),
     "dms_decode_attention": (_I, [_P, _P, _P, ctypes.c_float, _I, _P]),
+    "dms_prefill": (_I, [_P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _P]),
     "dms_cache_lengths": (_I, [_P, _P, _P]),
     "dms_cache_slot_positions": (_I, [_P, _P, _P]),
     "dms_cache_export_kv": (_I, [_P, _P, _P, _P]),
@@ -153,6 +154,27 @@ class DmsCache:
         _check(self._lib.dms_append_chunk(self.handle, k.data_ptr(), v.data_ptr(), logits.data_ptr(), C,
                                           _stream_handle(stream)), "dms_append_chunk")
 
+    def prefill(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, logits: torch.Tensor,
+                out: torch.Tensor | None = None, scale: float | None = None, stream=None) -> torch.Tensor:
+        """Attention of a chunk of C tokens over the cache and the chunk itself,
+        then the chunk's append (dms_prefill).  q [B][Hq][C][D] bf16, k/v
+        [B][Hkv][C][D] bf16, logits [B][Hkv][C] fp32 -> out [B][Hq][C][D] fp32."""
+        B, H, D = self.batch, self.kv_heads, self.head_dim
+        if q.dim() != 4:
+            raise ValueError("q must be [batch][q_heads][chunk][head_dim]")
+        Hq, C = q.shape[1], q.shape[2]
+        _need(q, "q", torch.bfloat16, (B, Hq, C, D), self.device)
+        _need(k, "k", torch.bfloat16, (B, H, C, D), self.device)
+        _need(v, "v", torch.bfloat16, (B, H, C, D), self.device)
+        _need(logits, "logits", torch.float32, (B, H, C), self.device)
+        if out is None:
+            out = torch.empty((B, Hq, C, D), dtype=torch.float32, device=self.device)
+        _need(out, "out", torch.float32, (B, Hq, C, D), self.device)
+        scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+        _check(self._lib.dms_prefill(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), logits.data_ptr(), C,
+                                     out.data_ptr(), scale, Hq, _stream_handle(stream)), "dms_prefill")
+        return out
+
     def decode_attention(self, q: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,
                          stream=None) -> torch.Tensor:
         B, D = self.batch, self.head_dim
@@ -204,6 +226,10 @@ def dms_append(cache: DmsCache, k, v, evict_logit, stream=None) -> None:
 
 def dms_append_chunk(cache: DmsCache, k, v, logits, stream=None) -> None:
     cache.append_chunk(k, v, logits, stream)
+
+
+def dms_prefill(cache: DmsCache, q, k, v, logits, out=None, scale=None, stream=None):
+    return cache.prefill(q, k, v, logits, out, scale, stream)
 
 
 def dms_decode_attention(cache: DmsCache, q, out=None, scale=None, stream=None):

@@ -159,9 +159,11 @@ def test_first_step_returns_first_value_exactly():
     assert torch.equal(out, expect)
 
 
-@pytest.mark.parametrize("chunk", [1, 7, 16, 33, 100])
-def test_chunk_append_equals_single_appends(chunk):
-    wl = _small("chunk", 3, 8, 4, 64, 16, 400, ("normal", 0.8, 1.0), seed=5)
+@pytest.mark.parametrize("chunk,w", [(1, 16), (7, 16), (16, 16), (33, 16), (100, 16), (33, 1), (100, 1), (64, 4)])
+def test_chunk_append_equals_single_appends(chunk, w):
+    """Chunked appends leave the cache byte-identical to single appends,
+    including chains where a token retires one of the same chunk (w < chunk)."""
+    wl = _small("chunk", 3, 8, 4, 64, w, 400, ("normal", 0.8, 1.0), seed=5)
     T = 350
     a = Trajectory(wl, T)
     b = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
