@@ -403,6 +403,87 @@ def cpu_baseline(wl, n_ctx, seconds=12.0, rows=(0, 1)):
                       f"{wl.B} at positions {n_ctx - min(steps, 256)}..{n_ctx - 1} ({steps} steps, {dt:.1f} s)"}
 
 
+def measured_bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1800.0, "fallback"
+
+
+def prefill_flops(wl, lens, t_ctx, C):
+    """Algorithmic flops of one chunk's attention: every (query row, key) pair
+    the rows may attend to -- the retained cache plus the chunk's causal prefix
+    -- costs 2 D for Q K^T and 2 D for P V."""
+    pairs = 0
+    for L in lens:  # per (sequence, KV head)
+        pairs += wl.G * (C * int(L) + C * (C + 1) // 2)
+    return 4 * wl.D * pairs
+
+
+def time_prefill_leg(dms, W, steps, device):
+    """The chunked prefill (a row of the hot path that the decode metric does not
+    cover): one layer of the long-context workload, chunks of 512 tokens at a
+    context of ~29-33K.  Times dms_prefill (attention + append) per chunk with
+    events, and dms_append_chunk alone on a twin cache at the same positions;
+    the difference is the attention kernel."""
+    wl = W.WORKLOADS["long-context"]
+    C = wl.chunk
+    n_end = wl.prefill
+    n0 = n_end - C * steps
+    lib = dms.load_library()
+    a = fill_cache(dms, W, wl, n0, device, layer=0)
+    b = fill_cache(dms, W, wl, n0, device, layer=0)
+    k, v, lg = W.kv_range(wl, 0, n0, n_end, device=device)
+    q = W.q_range(wl, 0, n0, n_end, device=device)
+    chunks = [(q[:, :, j * C:(j + 1) * C].contiguous(), k[:, :, j * C:(j + 1) * C].contiguous(),
+               v[:, :, j * C:(j + 1) * C].contiguous(), lg[:, :, j * C:(j + 1) * C].contiguous()) for j in range(steps)]
+    out = torch.empty((wl.B, wl.Hq, C, wl.D), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    t_pre, t_app, flops = [], [], 0
+    for j, (qq, kk, vv, ll) in enumerate(chunks):
+        lens = a.lengths().cpu().numpy().ravel()
+        flops_j = prefill_flops(wl, lens, n0 + j * C, C)
+        e0, e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+        e0.record(stream)
+        rc = lib.dms_prefill(a.handle, qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), ll.data_ptr(), C,
+                             out.data_ptr(), wl.scale, wl.Hq, sh)
+        e1.record(stream)
+        if rc:
+            raise dms.DmsError(rc, "dms_prefill")
+        e2.record(stream)
+        rc = lib.dms_append_chunk(b.handle, kk.data_ptr(), vv.data_ptr(), ll.data_ptr(), C, sh)
+        e3.record(stream)
+        if rc:
+            raise dms.DmsError(rc, "dms_append_chunk")
+        torch.cuda.synchronize(device)
+        if j >= 1:  # the first chunk is warm-up
+            t_pre.append(e0.elapsed_time(e1) * 1e3)
+            t_app.append(e2.elapsed_time(e3) * 1e3)
+            flops += flops_j
+    st = a.status()
+    if st != dms.DMS_OK:
+        raise dms.DmsError(st, "device status after the prefill leg")
+    a.close()
+    b.close()
+    n = len(t_pre)
+    pre_us, app_us = sum(t_pre) / n, sum(t_app) / n
+    attn_us = max(pre_us - app_us, 1e-3)
+    tflops = flops / n / (attn_us * 1e-6) / 1e12
+    peak, kind = measured_bf16_peak()
+    return {"workload": f"long-context layer: batch {wl.B}, {wl.Hq} query / {wl.Hkv} KV heads, head_dim {wl.D}, "
+                        f"chunks of {C} at context {n0 + C}..{n_end}",
+            "chunks_timed": n, "us_per_chunk_call": pre_us, "us_per_chunk_append": app_us,
+            "us_per_chunk_attention": attn_us, "tokens_per_s": wl.B * C / (pre_us * 1e-6),
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "peak_source": f"{kind} dense bf16 (burst)",
+                         "kernel": "prefill_attention_kernel (tcgen05)",
+                         "algorithmic_flops_per_chunk": flops / n,
+                         "flops_definition": "4 * head_dim per (query row, key) pair over the retained cache "
+                                             "and the chunk's causal prefix"}}
+
+
 def workload_config(wl, n_ctx):
     return {"workload": f"{wl.name} decode at context {n_ctx}: batch {wl.B}, {wl.Hq} query / {wl.Hkv} KV heads, "
                         f"head_dim {wl.D}, window {wl.w}, eviction logits {wl.logits}",
@@ -446,6 +527,7 @@ def main():
     ap.add_argument("--no-cr1", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -550,6 +632,8 @@ def main():
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "note": "Python API, pinned host inputs copied in and output copied out every step, "
                                "stream synchronized every step"}
+    if not args.no_prefill and world == 1:
+        line["prefill"] = time_prefill_leg(dms, W, 9, device)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, n_end)
     print(json.dumps(line), flush=True)
