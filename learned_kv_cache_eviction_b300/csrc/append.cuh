@@ -70,58 +70,129 @@ __global__ void __launch_bounds__(256) append_kernel(CacheView c, const uint4* _
   }
 }
 
-// `chunk` appends per (sequence, KV head) in position order, one warp per
-// head.  Lane 0 assigns the slots of up to 32 tokens at a time sequentially
-// (bit-identical to single appends, including chains where a token retires
-// another token of the same chunk); then the warp copies those rows, skipping
-// a row whose slot a later token of the same batch takes over (that token
-// retired it), so that no slot is written twice by one batch.
-// k, v: [NH][chunk][D/8] chunks; logits: [NH][chunk].
-template <int D>
-__global__ void __launch_bounds__(128) append_chunk_kernel(CacheView c, const uint4* __restrict__ k,
-                                                           const uint4* __restrict__ v,
-                                                           const float* __restrict__ logits, int64_t t0,
-                                                           int chunk) {
-  constexpr int CH = D / 8;
-  __shared__ int slots_smem[4][32];
+// Bookkeeping of `chunk` appends (positions t0 .. t0 + chunk - 1) per
+// (sequence, KV head), bit-identical to that many single appends; one warp per
+// head, 32 tokens at a time, lane j taking token base + j.
+//   * Token t retires token t - w if that one was stored and marked; it then
+//     takes its slot.  Lanes j and j + w of a batch depend on each other, lanes
+//     closer than w do not: the batch is resolved in runs of w lanes, each run
+//     with one ballot (which lanes need a fresh slot), a prefix count (their
+//     order) and two shuffles (the slot and mark of token t - w).
+//   * For w <= 32 the state of the tokens before a batch comes from the
+//     previous batch's lanes by shuffles; for larger w, and for the first
+//     batch, from the ring in memory.
+//   * Fresh slots are handed out in position order from len; beyond the
+//     capacity a token is dropped (ring entry "no slot, keep") and the
+//     capacity error is latched, as for a single append.
+// The slot -> position map, the ring and len are written here; the K/V rows
+// are copied by append_chunk_copy_kernel from the final slot -> position map.
+__global__ void __launch_bounds__(128) append_chunk_slots_kernel(CacheView c, const float* __restrict__ logits,
+                                                                 int64_t t0, int chunk) {
   griddep_wait();
   griddep_launch_dependents();
-  const int wl = threadIdx.x >> 5;
-  const int i = static_cast<int>(blockIdx.x * 4 + wl);
+  const int i = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (i >= c.NH) return;
-  int* slots = slots_smem[wl];
-  int len_reg = c.len[i];
+  const int w = c.w;
+  int32_t* rs = c.ring_slot + static_cast<size_t>(i) * w;
+  uint8_t* rf = c.ring_flag + static_cast<size_t>(i) * w;
+  int32_t* sp = c.slot_pos + static_cast<size_t>(i) * c.cap;
+  int len = c.len[i];
+  bool overflow = false;
+  int slot = -1, flag = 0;  // this lane's token in the current (then previous) batch
   for (int base = 0; base < chunk; base += 32) {
     const int n = min(32, chunk - base);
-    if (lane == 0) {
-      for (int j = 0; j < n; ++j) {
-        const float lg = logits[static_cast<size_t>(i) * chunk + base + j];
-        const int s = append_bookkeeping(c, i, t0 + base + j, lg, len_reg);
-        slots[j] = s;
-        // Token j took the slot of token j - w (which it retired): if that token
-        // is in this batch, it is not copied, so the slot is written once.
-        if (s >= 0 && j >= c.w && slots[j - c.w] == s) slots[j - c.w] = -1;
-      }
+    const bool active = lane < n;
+    const int64_t t = t0 + base + lane;
+    const bool marked = active && logits[static_cast<size_t>(i) * chunk + base + lane] > 0.0f;
+    // Token t - w for lanes where it precedes this batch (lane < w).
+    int rslot = -1, rflag = 0;
+    if (w <= 32 && base > 0) {  // the previous batch was full: t - w was its lane 32 - w + lane
+      rslot = __shfl_sync(0xffffffffu, slot, (lane + 32 - w) & 31);
+      rflag = __shfl_sync(0xffffffffu, flag, (lane + 32 - w) & 31);
+    } else if (active && lane < w && t >= w) {
+      const int r = static_cast<int>(t % w);
+      rslot = rs[r];
+      rflag = rf[r];
     }
-    __syncwarp();
-    // n rows x (CH K chunks + CH V chunks)
-    for (int idx = lane; idx < n * 2 * CH; idx += 32) {
-      const int j = idx / (2 * CH);
-      const int q = idx % (2 * CH);
-      const int s = slots[j];
-      if (s < 0) continue;
-      const size_t src = (static_cast<size_t>(i) * chunk + base + j) * CH;
-      const size_t row = (static_cast<size_t>(i) * c.cap + s) * CH;
-      if (q < CH) {
-        c.K[row + (q ^ (s & 7))] = __ldg(k + src + q);
-      } else {
-        c.V[row + (q - CH)] = __ldg(v + src + (q - CH));
+    slot = -1;
+    flag = 0;
+    for (int sb = 0; sb < n; sb += w) {  // run of lanes [sb, sb + w)
+      const bool in_run = active && lane >= sb && lane < sb + w;
+      const int src = lane >= w ? lane - w : 0;
+      const int pslot = __shfl_sync(0xffffffffu, slot, src);
+      const int pflag = __shfl_sync(0xffffffffu, flag, src);
+      bool retire = false;
+      int rslot_eff = -1;
+      if (t >= w) {
+        retire = (lane >= w ? pflag : rflag) != 0;
+        rslot_eff = lane >= w ? pslot : rslot;
       }
+      const bool fresh = in_run && !retire;
+      const unsigned m = __ballot_sync(0xffffffffu, fresh);
+      const int rank = __popc(m & ((1u << lane) - 1u));
+      const int room = c.cap - len;
+      if (in_run) {
+        slot = retire ? rslot_eff : (rank < room ? len + rank : -1);
+        flag = (slot >= 0 && marked) ? 1 : 0;
+      }
+      const int nf = __popc(m);
+      if (nf > room) overflow = true;
+      len += min(nf, room);
+    }
+    // A lane whose slot lane + w of this batch took (it retired this token) does
+    // not record its position; the later token's entry is the one that stays.
+    const int nxt = __shfl_sync(0xffffffffu, slot, (lane + w) & 31);
+    const bool superseded = w < 32 && lane + w < n && slot >= 0 && nxt == slot;
+    if (active && slot >= 0 && !superseded) sp[slot] = static_cast<int32_t>(t);
+    // The ring keeps the last w tokens: each batch writes the entries of its
+    // lanes that no later lane of the batch overwrites.
+    if (active && lane + w >= n) {
+      const int r = static_cast<int>(t % w);
+      rs[r] = slot;
+      rf[r] = static_cast<uint8_t>(flag);
     }
     __syncwarp();
   }
-  if (lane == 0) c.len[i] = len_reg;
+  if (lane == 0) {
+    c.len[i] = len;
+    if (overflow) atomicOr(c.err, kErrBitCapacity);
+  }
+}
+
+// K/V rows of a chunk appended by append_chunk_slots_kernel: every slot whose
+// final position lies in [t0, t0 + chunk) receives that token's row (a token
+// retired within the same chunk is no longer in the map, so each slot is
+// written once).  Grid: (slot groups of 256, heads); one warp per 32 slots,
+// one coalesced row (K chunks permuted by slot, then V) per step.
+template <int D>
+__global__ void __launch_bounds__(256) append_chunk_copy_kernel(CacheView c, const uint4* __restrict__ k,
+                                                                const uint4* __restrict__ v, int64_t t0,
+                                                                int chunk) {
+  constexpr int CH = D / 8;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int i = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  const int s0 = (static_cast<int>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * 32;
+  const int L = c.len[i];
+  if (s0 >= L) return;
+  const int s = s0 + lane;
+  const int p = s < L ? c.slot_pos[static_cast<size_t>(i) * c.cap + s] : -1;
+  unsigned m = __ballot_sync(0xffffffffu, p >= t0 && p < t0 + chunk);
+  while (m) {
+    const int src = __ffs(m) - 1;
+    m &= m - 1;
+    const int ss = s0 + src;
+    const int tok = __shfl_sync(0xffffffffu, p, src) - static_cast<int>(t0);
+    const size_t in = (static_cast<size_t>(i) * chunk + tok) * CH;
+    const size_t row = (static_cast<size_t>(i) * c.cap + ss) * CH;
+    if (lane < CH) {
+      c.K[row + (lane ^ (ss & 7))] = __ldg(k + in + lane);
+    } else if (lane < 2 * CH) {
+      c.V[row + lane - CH] = __ldg(v + in + lane - CH);
+    }
+  }
 }
 
 // Logical-order copy of the K and V pools (undoes the chunk permutation of K).

@@ -176,14 +176,18 @@ int launch_prefill_d(dms_cache* c, const dms::PrefillArgs& a, int G, cudaStream_
   }
 }
 
+// Chunk append: the bookkeeping (one warp per head), then the row copy.
 int launch_append_chunk(dms_cache* c, const void* k, const void* v, const float* logits, int chunk, cudaStream_t st) {
-  const int blocks = (c->NH + 3) / 4;
+  const int rc = launch_pdl(dms::append_chunk_slots_kernel, dim3((c->NH + 3) / 4), dim3(128), 0, st, c->view, logits,
+                            c->t, chunk);
+  if (rc != DMS_OK) return rc;
+  const dim3 grid((c->cap + 255) / 256, c->NH);
   const uint4* k4 = static_cast<const uint4*>(k);
   const uint4* v4 = static_cast<const uint4*>(v);
-  return c->D == 128 ? launch_pdl(dms::append_chunk_kernel<128>, dim3(blocks), dim3(128), 0, st, c->view, k4, v4,
-                                  logits, c->t, chunk)
-                     : launch_pdl(dms::append_chunk_kernel<64>, dim3(blocks), dim3(128), 0, st, c->view, k4, v4,
-                                  logits, c->t, chunk);
+  return c->D == 128 ? launch_pdl(dms::append_chunk_copy_kernel<128>, grid, dim3(256), 0, st, c->view, k4, v4, c->t,
+                                  chunk)
+                     : launch_pdl(dms::append_chunk_copy_kernel<64>, grid, dim3(256), 0, st, c->view, k4, v4, c->t,
+                                  chunk);
 }
 
 void free_cache_memory(dms_cache* c) {

@@ -13,8 +13,9 @@
 //   * a cached token marked for eviction is still in the cache only if it is
 //     among the last w positions before t0 (its ring entry carries the mark);
 //   * a chunk token's mark is its logit > 0.
-// The chunk is appended to the cache afterwards (append_chunk_kernel), so the
-// whole call equals C rounds of single-token append + decode attention.
+// The chunk is appended to the cache afterwards (append_chunk_slots_kernel,
+// append_chunk_copy_kernel), so the whole call equals C rounds of single-token
+// append + decode attention.
 //
 // One CTA of 128 threads per (tile of PT = 128 / G query positions x G query
 // heads, KV head).  Row r of the tile is query head g = r / PT at chunk

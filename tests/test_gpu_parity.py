@@ -159,7 +159,8 @@ def test_first_step_returns_first_value_exactly():
     assert torch.equal(out, expect)
 
 
-@pytest.mark.parametrize("chunk,w", [(1, 16), (7, 16), (16, 16), (33, 16), (100, 16), (33, 1), (100, 1), (64, 4)])
+@pytest.mark.parametrize("chunk,w", [(1, 16), (7, 16), (16, 16), (33, 16), (100, 16), (33, 1), (100, 1), (64, 4),
+                                     (70, 32), (33, 40), (100, 40), (37, 5)])
 def test_chunk_append_equals_single_appends(chunk, w):
     """Chunked appends leave the cache byte-identical to single appends,
     including chains where a token retires one of the same chunk (w < chunk)."""
@@ -183,6 +184,27 @@ def test_chunk_append_equals_single_appends(chunk, w):
     assert torch.equal(ka, kb) and torch.equal(va, vb)
     a.check_kv()
     assert b.position == a.cache.position == T
+
+
+@pytest.mark.parametrize("w", [3, 16, 40])
+def test_chunk_append_capacity_overflow_matches_single_appends(w):
+    """A chunk that runs past the capacity leaves the same state as single
+    appends (dropped tokens keep no slot) and latches the capacity error."""
+    wl = _small("capchunk", 2, 4, 2, 64, w, 20, ("normal", -0.5, 1.0), seed=9)
+    T = 90
+    a = Trajectory(wl, T)
+    b = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
+    a.append_chunk(T)
+    for t in range(T):
+        b.append(a.k[:, :, t].contiguous().cuda(), a.v[:, :, t].contiguous().cuda(), a.lg[:, :, t].contiguous().cuda())
+    assert a.sim.overflow
+    assert a.cache.status() == b.status() == dms.DMS_ERR_CAPACITY
+    a.check_lengths()
+    a.check_slots()
+    assert torch.equal(a.cache.slot_positions(), b.slot_positions())
+    ka, va = a.cache.export_kv()
+    kb, vb = b.export_kv()
+    assert torch.equal(ka, kb) and torch.equal(va, vb)
 
 
 def test_capacity_overflow_is_reported():
