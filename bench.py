@@ -528,6 +528,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="run only the prefill leg and print its figures (for profiling)")
+    ap.add_argument("--prefill-chunks", type=int, default=9)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -545,6 +548,13 @@ def main():
         return
 
     from learned_kv_cache_eviction_b300 import dms
+
+    if args.prefill_only:
+        device = torch.device("cuda", local_rank)
+        torch.cuda.set_device(device)
+        print(json.dumps({"impl": "native", "prefill": time_prefill_leg(dms, W, args.prefill_chunks, device)}),
+              flush=True)
+        return
 
     dist = None
     if world > 1:
@@ -633,7 +643,7 @@ def main():
                        "note": "Python API, pinned host inputs copied in and output copied out every step, "
                                "stream synchronized every step"}
     if not args.no_prefill and world == 1:
-        line["prefill"] = time_prefill_leg(dms, W, 9, device)
+        line["prefill"] = time_prefill_leg(dms, W, args.prefill_chunks, device)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, n_end)
     print(json.dumps(line), flush=True)

@@ -150,6 +150,12 @@ int launch_prefill_t(dms_cache* c, const dms::PrefillArgs& a, cudaStream_t st) {
   using Sh = dms::PrefillShape<D, G>;
   static bool attr_done[64] = {};
   if (c->device < 64 && !attr_done[c->device]) {
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device) != cudaSuccess ||
+        optin < Sh::SMEM + 1024) {  // dynamic + the kernel's 1 KB of static shared memory
+      cudaGetLastError();
+      return DMS_ERR_CUDA;
+    }
     if (cudaFuncSetAttribute(dms::prefill_attention_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Sh::SMEM) != cudaSuccess) {
       cudaGetLastError();

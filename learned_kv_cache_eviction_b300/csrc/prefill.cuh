@@ -25,6 +25,8 @@
 //   1. the threads stage the K and V tile in shared memory in the 128-byte
 //      swizzled layouts (K rows of the cache pool are stored chunk-permuted by
 //      slot, which is that layout already), plus each key's (position, last);
+//      K, V and the metadata are double-buffered: the next tile's asynchronous
+//      copies (cp.async) are in flight while this one is computed;
 //   2. one thread issues S = Q K^T (bf16 x bf16 -> fp32 in tensor memory);
 //   3. every thread loads its row of S, masks it, and updates the running
 //      max (only when it grows by more than 2^8, rescaling the accumulator in
@@ -32,7 +34,7 @@
 //      terms, hi = bf16(p) and lo = bf16(p - hi), so that P V keeps ~16 bits
 //      of p;
 //   4. one thread issues O += P_hi V + P_lo V (fp32 in tensor memory).
-// The steps are serialised on two mbarriers; every wait has a time limit.
+// The MMAs are ordered on two mbarriers; every wait has a time limit.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -53,12 +55,12 @@ struct PrefillShape {
   static constexpr int NP = D / 64;                      // 128-byte panels per row of Q, K, V
   static constexpr int PANEL = 128 * 128;                // bytes of one panel of 128 rows
   static constexpr int OFF_Q = 0;                        // Q: NP panels, K-major
-  static constexpr int OFF_K = OFF_Q + NP * PANEL;       // K: NP panels, K-major (B of S = Q K^T)
-  static constexpr int OFF_V = OFF_K + NP * PANEL;       // V: NP panels, MN-major (B of O = P V)
-  static constexpr int OFF_PH = OFF_V + NP * PANEL;      // P hi: 2 panels (128 keys), K-major
+  static constexpr int OFF_K = OFF_Q + NP * PANEL;       // K: 2 buffers x NP panels, K-major (B of S = Q K^T)
+  static constexpr int OFF_V = OFF_K + 2 * NP * PANEL;   // V: 2 buffers x NP panels, MN-major (B of O = P V)
+  static constexpr int OFF_PH = OFF_V + 2 * NP * PANEL;  // P hi: 2 panels (128 keys), K-major
   static constexpr int OFF_PL = OFF_PH + 2 * PANEL;      // P lo
-  static constexpr int OFF_META = OFF_PL + 2 * PANEL;    // int2 [NK]: (position, last visible position)
-  static constexpr int SMEM = OFF_META + NK * 8;
+  static constexpr int OFF_META = OFF_PL + 2 * PANEL;    // 2 buffers x int2 [NK]: (position, last visible)
+  static constexpr int SMEM = OFF_META + 2 * NK * 8;     // 227 KB at head_dim 128
   static constexpr int TMEM_S = 0;                       // S: columns [0, NK)
   static constexpr int TMEM_O = NK;                      // O: columns [NK, NK + D)
   static constexpr uint32_t TMEM_COLS = 256;
@@ -92,11 +94,11 @@ __global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const Prefill
   __shared__ __align__(8) uint64_t bar_o;
   __shared__ uint32_t tmem_base;
   uint8_t* sQ = smem + Sh::OFF_Q;
-  uint8_t* sK = smem + Sh::OFF_K;
-  uint8_t* sV = smem + Sh::OFF_V;
+  uint8_t* sK0 = smem + Sh::OFF_K;
+  uint8_t* sV0 = smem + Sh::OFF_V;
   uint8_t* sPH = smem + Sh::OFF_PH;
   uint8_t* sPL = smem + Sh::OFF_PL;
-  int2* meta = reinterpret_cast<int2*>(smem + Sh::OFF_META);
+  int2* meta0 = reinterpret_cast<int2*>(smem + Sh::OFF_META);
   const int tid = threadIdx.x, warp = tid >> 5;
   const int i = blockIdx.y;  // (sequence, KV head)
   const int b = i / a.Hkv, h = i - b * a.Hkv;
@@ -146,8 +148,58 @@ __global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const Prefill
   int w_s = 0, w_o = 0;                       // of which waited for
   bool failed = false;
 
+  // Tile it: keys [k0, k0 + kn) of the cache's retained slots (it < nkc) or of
+  // the chunk.  K and V tiles go to buffer it & 1 with asynchronous 16-byte
+  // copies (rows past kn are zero-filled); cache K rows already hold chunk c at
+  // c ^ (slot & 7), and slot & 7 == j & 7 because tiles start at multiples of
+  // 128, so their swizzled position is c itself.
+  auto stage = [&](int t) {
+    const bool from_cache = t < nkc;
+    const int k0 = from_cache ? t * NK : (t - nkc) * NK;
+    const int kn = from_cache ? min(NK, L - k0) : min(NK, kend - k0);
+    uint8_t* dK = sK0 + (t & 1) * (Sh::NP * PANEL);
+    uint8_t* dV = sV0 + (t & 1) * (Sh::NP * PANEL);
+    const uint4* gK = from_cache ? a.K + static_cast<size_t>(i) * a.cap * CH : a.kc + static_cast<size_t>(i) * a.C * CH;
+    const uint4* gV = from_cache ? a.V + static_cast<size_t>(i) * a.cap * CH : a.vc + static_cast<size_t>(i) * a.C * CH;
+#pragma unroll 4
+    for (int x = tid; x < NK * CH; x += 128) {
+      const int j = x / CH, cc = x % CH;
+      const bool ok = j < kn;
+      const size_t src = ok ? static_cast<size_t>(k0 + j) * CH + cc : 0;
+      const int kpos = from_cache ? (cc & 7) : ((cc & 7) ^ (j & 7));
+      umma::cp_async16(dK + (cc >> 3) * PANEL + j * 128 + (kpos << 4), gK + src, ok);
+      umma::cp_async16(dV + (cc >> 3) * PANEL + j * 128 + (((cc & 7) ^ (j & 7)) << 4), gV + src, ok);
+    }
+  };
+  // Key metadata of tile t into buffer t & 1: (position, last visible position).
+  auto stage_meta = [&](int t) {
+    const bool from_cache = t < nkc;
+    const int k0 = from_cache ? t * NK : (t - nkc) * NK;
+    const int kn = from_cache ? min(NK, L - k0) : min(NK, kend - k0);
+    const int j = tid;  // NK == blockDim.x
+    int pos = INT_MAX, last = -1;  // invisible
+    if (j < kn) {
+      if (from_cache) {
+        pos = a.slot_pos[static_cast<size_t>(i) * a.cap + k0 + j];
+        const bool marked = pos >= pend_lo && a.ring_flag[static_cast<size_t>(i) * a.w + pos % a.w] != 0;
+        last = marked ? pos + a.w - 1 : INT_MAX;
+      } else {
+        pos = a.t0 + k0 + j;
+        const bool marked = a.logits[static_cast<size_t>(i) * a.C + k0 + j] > 0.0f;
+        last = marked ? pos + a.w - 1 : INT_MAX;
+      }
+    }
+    meta0[(t & 1) * NK + j] = make_int2(pos, last);
+  };
+  if (ntiles > 0) {
+    stage(0);
+    umma::cp_async_commit();
+    stage_meta(0);
+  }
+
   for (int it = 0; it < ntiles; ++it) {
-    // The previous P V must be done: it reads the V and P tiles and writes O.
+    // The previous P V must be done: it reads the V and P tiles (and the K/V
+    // buffer refilled below held tile it - 1) and writes O.
     if (w_o < n_o) {
       const bool ok = mbar_wait(&bar_o, w_o & 1);
       ++w_o;
@@ -157,41 +209,13 @@ __global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const Prefill
       }
       umma::fence_after_sync();
     }
-    // ---- 1. K, V tile and key metadata ----
-    const bool from_cache = it < nkc;
-    const int k0 = from_cache ? it * NK : (it - nkc) * NK;
-    const int kn = from_cache ? min(NK, L - k0) : min(NK, kend - k0);
-    for (int x = tid; x < NK * CH; x += 128) {
-      const int j = x / CH, cc = x % CH;
-      uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
-      if (j < kn) {
-        const size_t row = from_cache ? (static_cast<size_t>(i) * a.cap + k0 + j) * CH
-                                      : (static_cast<size_t>(i) * a.C + k0 + j) * CH;
-        kv = __ldg((from_cache ? a.K : a.kc) + row + cc);
-        vv = __ldg((from_cache ? a.V : a.vc) + row + cc);
-      }
-      // Cache K rows already hold chunk c at c ^ (slot & 7), and slot & 7 == j & 7
-      // because tiles start at multiples of 128: the swizzled position is cc.
-      const int kpos = from_cache ? (cc & 7) : ((cc & 7) ^ (j & 7));
-      *reinterpret_cast<uint4*>(sK + (cc >> 3) * PANEL + j * 128 + (kpos << 4)) = kv;
-      *reinterpret_cast<uint4*>(sV + (cc >> 3) * PANEL + j * 128 + (((cc & 7) ^ (j & 7)) << 4)) = vv;
-    }
-    {
-      const int j = tid;  // NK == blockDim.x
-      int pos = INT_MAX, last = -1;  // invisible
-      if (j < kn) {
-        if (from_cache) {
-          pos = a.slot_pos[static_cast<size_t>(i) * a.cap + k0 + j];
-          const bool marked = pos >= pend_lo && a.ring_flag[static_cast<size_t>(i) * a.w + pos % a.w] != 0;
-          last = marked ? pos + a.w - 1 : INT_MAX;
-        } else {
-          pos = a.t0 + k0 + j;
-          const bool marked = a.logits[static_cast<size_t>(i) * a.C + k0 + j] > 0.0f;
-          last = marked ? pos + a.w - 1 : INT_MAX;
-        }
-      }
-      meta[j] = make_int2(pos, last);
-    }
+    // ---- 1. prefetch tile it + 1, then wait for tile it's copies ----
+    if (it + 1 < ntiles) stage(it + 1);
+    umma::cp_async_commit();
+    umma::cp_async_wait_prior();
+    const uint8_t* sK = sK0 + (it & 1) * (Sh::NP * PANEL);
+    const uint8_t* sV = sV0 + (it & 1) * (Sh::NP * PANEL);
+    const int2* meta = meta0 + (it & 1) * NK;
     umma::fence_proxy_async_smem();
     umma::fence_before_sync();
     __syncthreads();
@@ -209,6 +233,7 @@ __global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const Prefill
       umma::commit(&bar_s);
     }
     ++n_s;
+    if (it + 1 < ntiles) stage_meta(it + 1);  // overlaps the S MMA
     {
       const bool ok = mbar_wait(&bar_s, w_s & 1);
       ++w_s;
@@ -323,6 +348,7 @@ __global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const Prefill
   }
   if (failed) {
     if (tid == 0) atomicOr(a.err, kErrBitTimeout);
+    umma::cp_async_wait_all();
     // Wait (bounded) for the tensor-core work still in flight before freeing its memory.
     for (; w_s < n_s; ++w_s) (void)mbar_wait(&bar_s, w_s & 1);
     for (; w_o < n_o; ++w_o) (void)mbar_wait(&bar_o, w_o & 1);

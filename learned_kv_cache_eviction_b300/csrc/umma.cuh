@@ -1,7 +1,8 @@
 // umma.cuh -- 5th-generation tensor core (tcgen05) helpers for sm_103a, as
 // inline PTX: tensor-memory allocation, shared-memory matrix descriptors,
 // instruction descriptors, MMA issue and commit, and tensor-memory loads and
-// stores.  Used by the chunked-prefill attention kernel (prefill.cuh).
+// stores, and asynchronous global -> shared copies.  Used by the
+// chunked-prefill attention kernel (prefill.cuh).
 //
 // Layout conventions (all operand tiles in shared memory use the 128-byte
 // swizzle): a "panel" is 128 bytes wide; within a 1024-byte atom of 8 rows,
@@ -58,6 +59,18 @@ __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence
 // Make this thread's generic-proxy shared-memory writes visible to the tensor
 // core (async proxy).
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Asynchronous 16-byte copy global -> shared (cp.async, L2 only); with
+// valid == false nothing is read and the 16 bytes are zero-filled.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most one committed group of this thread is still in flight.
+__device__ __forceinline__ void cp_async_wait_prior() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // D[tmem] (+)= A[smem] x B[smem]; issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
