@@ -164,7 +164,7 @@ int launch_prefill_t(dms_cache* c, const dms::PrefillArgs& a, cudaStream_t st) {
     attr_done[c->device] = true;
   }
   const dim3 grid((a.C + Sh::PT - 1) / Sh::PT, c->NH);
-  return launch_pdl(dms::prefill_attention_kernel<D, G>, grid, dim3(128), Sh::SMEM, st, a);
+  return launch_pdl(dms::prefill_attention_kernel<D, G>, grid, dim3(256), Sh::SMEM, st, a);
 }
 
 template <int D>

@@ -17,9 +17,11 @@
 // append_chunk_copy_kernel), so the whole call equals C rounds of single-token
 // append + decode attention.
 //
-// One CTA of 128 threads per (tile of PT = 128 / G query positions x G query
+// One CTA of 256 threads per (tile of PT = 128 / G query positions x G query
 // heads, KV head).  Row r of the tile is query head g = r / PT at chunk
-// position c0 + r % PT; thread r owns row r (tensor-memory lane r).  For each
+// position c0 + r % PT, tensor-memory lane r; threads r and r + 128 share row
+// r (the two warps of a lane quarter), each owning half of its keys in the
+// softmax and half of its output columns.  For each
 // tile of 128 keys (the cache's retained slots first, then the chunk's keys up
 // to the tile's last position):
 //   1. the threads stage the K and V tile in shared memory in the 128-byte
@@ -28,9 +30,11 @@
 //      K, V and the metadata are double-buffered: the next tile's asynchronous
 //      copies (cp.async) are in flight while this one is computed;
 //   2. one thread issues S = Q K^T (bf16 x bf16 -> fp32 in tensor memory);
-//   3. every thread loads its row of S, masks it, and updates the running
-//      max (only when it grows by more than 2^8, rescaling the accumulator in
-//      tensor memory then) and sum; p = 2^(s - m) is written as two bf16
+//   3. both threads of a row load the whole row of S, mask it and find its
+//      max (so they take the same decisions without talking); the running max
+//      moves only when it grows by more than 2^8 (the accumulator in tensor
+//      memory is rescaled then); each thread turns its 64 keys into
+//      p = 2^(s - m) and keeps its half of the row sum; p is written as two bf16
 //      terms, hi = bf16(p) and lo = bf16(p - hi), so that P V keeps ~16 bits
 //      of p;
 //   4. one thread issues O += P_hi V + P_lo V (fp32 in tensor memory).
@@ -61,9 +65,9 @@ struct PrefillShape {
   static constexpr int OFF_PL = OFF_PH + 2 * PANEL;      // P lo
   static constexpr int OFF_META = OFF_PL + 2 * PANEL;    // 2 buffers x int2 [NK]: (position, last visible)
   static constexpr int SMEM = OFF_META + 2 * NK * 8;     // 227 KB at head_dim 128
-  static constexpr int TMEM_S = 0;                       // S: columns [0, NK)
-  static constexpr int TMEM_O = NK;                      // O: columns [NK, NK + D)
-  static constexpr uint32_t TMEM_COLS = 256;
+  static constexpr int TMEM_S = 0;                       // S: 2 buffers, columns [0, 2 NK)
+  static constexpr int TMEM_O = 2 * NK;                  // O: columns [2 NK, 2 NK + D)
+  static constexpr uint32_t TMEM_COLS = 512;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(G >= 1 && G <= 8, "1 <= G <= 8");
 };
@@ -86,7 +90,7 @@ struct PrefillArgs {
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const PrefillArgs a) {
+__global__ void __launch_bounds__(256, 1) prefill_attention_kernel(const PrefillArgs a) {
   using Sh = PrefillShape<D, G>;
   constexpr int NK = Sh::NK, PT = Sh::PT, ROWS = Sh::ROWS, CH = D / 8, PANEL = Sh::PANEL;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -117,7 +121,7 @@ __global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const Prefill
     fence_barrier_init();
   }
   // Q tile: row r = (head g = r / PT, chunk position c0 + r % PT); unused rows are zero.
-  for (int x = tid; x < 128 * CH; x += 128) {
+  for (int x = tid; x < 128 * CH; x += 256) {
     const int r = x / CH, cc = x % CH;
     const int g = r / PT, c = c0 + r % PT;
     uint4 val = make_uint4(0u, 0u, 0u, 0u);
@@ -129,10 +133,10 @@ __global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const Prefill
   __syncthreads();
   umma::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's lanes
+  const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // this warp's lanes
 
-  // This thread's row.
-  const int r = tid;
+  // This thread's row, and which half of its columns (keys, then outputs) it owns.
+  const int r = tid & 127, hh = tid >> 7;
   const int rg = r / PT, rc = c0 + r % PT;
   const bool row_ok = r < ROWS && rc < a.C;
   const int tq = a.t0 + rc;  // the row's query position
@@ -144,96 +148,134 @@ __global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const Prefill
   const int nkk = (kend + NK - 1) / NK;       // tiles of chunk keys
   const int ntiles = nkc + nkk;
   const int pend_lo = a.t0 - a.w;             // cached positions >= this may still carry a mark
+  const int tq_first = a.t0 + c0;                          // query positions of the CTA's rows
+  const int tq_last = a.t0 + min(a.C, c0 + PT) - 1;
+  bool nomask_next = false;                   // tile-wide "no mask" flag of the next tile (uniform)
   int n_s = 0, n_o = 0;                       // commits issued on bar_s / bar_o (uniform)
   int w_s = 0, w_o = 0;                       // of which waited for
   bool failed = false;
 
-  // Tile it: keys [k0, k0 + kn) of the cache's retained slots (it < nkc) or of
-  // the chunk.  K and V tiles go to buffer it & 1 with asynchronous 16-byte
+  // Tile t: keys [k0, k0 + kn) of the cache's retained slots (t < nkc) or of
+  // the chunk.  Its K and V go to buffers t & 1 with asynchronous 16-byte
   // copies (rows past kn are zero-filled); cache K rows already hold chunk c at
   // c ^ (slot & 7), and slot & 7 == j & 7 because tiles start at multiples of
-  // 128, so their swizzled position is c itself.
-  auto stage = [&](int t) {
+  // 128, so their swizzled position is c itself.  K and V are staged
+  // separately: a K buffer is free once its S = Q K^T is done, a V buffer only
+  // once its P V is.
+  auto tile_keys = [&](int t, int& k0, int& kn) -> bool {
     const bool from_cache = t < nkc;
-    const int k0 = from_cache ? t * NK : (t - nkc) * NK;
-    const int kn = from_cache ? min(NK, L - k0) : min(NK, kend - k0);
-    uint8_t* dK = sK0 + (t & 1) * (Sh::NP * PANEL);
-    uint8_t* dV = sV0 + (t & 1) * (Sh::NP * PANEL);
-    const uint4* gK = from_cache ? a.K + static_cast<size_t>(i) * a.cap * CH : a.kc + static_cast<size_t>(i) * a.C * CH;
-    const uint4* gV = from_cache ? a.V + static_cast<size_t>(i) * a.cap * CH : a.vc + static_cast<size_t>(i) * a.C * CH;
+    k0 = from_cache ? t * NK : (t - nkc) * NK;
+    kn = from_cache ? min(NK, L - k0) : min(NK, kend - k0);
+    return from_cache;
+  };
+  auto stage_rows = [&](int t, bool is_v) {
+    int k0, kn;
+    const bool from_cache = tile_keys(t, k0, kn);
+    uint8_t* dst = (is_v ? sV0 : sK0) + (t & 1) * (Sh::NP * PANEL);
+    const uint4* g = is_v ? (from_cache ? a.V : a.vc) : (from_cache ? a.K : a.kc);
+    g += static_cast<size_t>(i) * (from_cache ? a.cap : a.C) * CH;
+    const bool pre_swizzled = from_cache && !is_v;
 #pragma unroll 4
-    for (int x = tid; x < NK * CH; x += 128) {
+    for (int x = tid; x < NK * CH; x += 256) {
       const int j = x / CH, cc = x % CH;
       const bool ok = j < kn;
       const size_t src = ok ? static_cast<size_t>(k0 + j) * CH + cc : 0;
-      const int kpos = from_cache ? (cc & 7) : ((cc & 7) ^ (j & 7));
-      umma::cp_async16(dK + (cc >> 3) * PANEL + j * 128 + (kpos << 4), gK + src, ok);
-      umma::cp_async16(dV + (cc >> 3) * PANEL + j * 128 + (((cc & 7) ^ (j & 7)) << 4), gV + src, ok);
+      const int pos = pre_swizzled ? (cc & 7) : ((cc & 7) ^ (j & 7));
+      umma::cp_async16(dst + (cc >> 3) * PANEL + j * 128 + (pos << 4), g + src, ok);
     }
   };
   // Key metadata of tile t into buffer t & 1: (position, last visible position).
-  auto stage_meta = [&](int t) {
-    const bool from_cache = t < nkc;
-    const int k0 = from_cache ? t * NK : (t - nkc) * NK;
-    const int kn = from_cache ? min(NK, L - k0) : min(NK, kend - k0);
-    const int j = tid;  // NK == blockDim.x
-    int pos = INT_MAX, last = -1;  // invisible
-    if (j < kn) {
+  // Split in two so that the loads of meta_begin are in flight while the
+  // softmax of the current tile runs: a key's position (and, for a chunk key,
+  // its logit) first; then, in meta_end, the ring lookup that only cached keys
+  // among the last w positions need, and the store.
+  auto meta_begin = [&](int t, int& pos, float& lg) {
+    int k0, kn;
+    const bool from_cache = tile_keys(t, k0, kn);
+    const int j = tid;  // threads [0, NK) handle one key each
+    pos = INT_MAX;
+    lg = 0.f;
+    if (j < NK && j < kn) {
       if (from_cache) {
         pos = a.slot_pos[static_cast<size_t>(i) * a.cap + k0 + j];
-        const bool marked = pos >= pend_lo && a.ring_flag[static_cast<size_t>(i) * a.w + pos % a.w] != 0;
-        last = marked ? pos + a.w - 1 : INT_MAX;
       } else {
         pos = a.t0 + k0 + j;
-        const bool marked = a.logits[static_cast<size_t>(i) * a.C + k0 + j] > 0.0f;
-        last = marked ? pos + a.w - 1 : INT_MAX;
+        lg = a.logits[static_cast<size_t>(i) * a.C + k0 + j];
       }
     }
-    meta0[(t & 1) * NK + j] = make_int2(pos, last);
   };
-  if (ntiles > 0) {
-    stage(0);
-    umma::cp_async_commit();
-    stage_meta(0);
-  }
-
-  for (int it = 0; it < ntiles; ++it) {
-    // The previous P V must be done: it reads the V and P tiles (and the K/V
-    // buffer refilled below held tile it - 1) and writes O.
-    if (w_o < n_o) {
-      const bool ok = mbar_wait(&bar_o, w_o & 1);
-      ++w_o;
-      if (__syncthreads_or(!ok)) {
-        failed = true;
-        break;
-      }
-      umma::fence_after_sync();
+  // Returns whether this key is a key of the tile that every row of the CTA
+  // sees (or lies past the tile's end), for the tile-wide "no mask" test.
+  auto meta_end = [&](int t, int pos, float lg) -> bool {
+    if (tid >= NK) return true;
+    int k0, kn;
+    const bool from_cache = tile_keys(t, k0, kn);
+    int last = -1;  // invisible unless set below
+    if (pos != INT_MAX) {
+      const bool marked = from_cache
+                              ? (pos >= pend_lo && a.ring_flag[static_cast<size_t>(i) * a.w + pos % a.w] != 0)
+                              : lg > 0.0f;
+      last = marked ? pos + a.w - 1 : INT_MAX;
     }
-    // ---- 1. prefetch tile it + 1, then wait for tile it's copies ----
-    if (it + 1 < ntiles) stage(it + 1);
+    meta0[(t & 1) * NK + tid] = make_int2(pos, last);
+    return tid >= kn || (pos <= tq_first && last >= tq_last);
+  };
+  auto issue_s = [&](int t) {  // S(t) = Q K(t)^T into S buffer t & 1; one thread
+    constexpr uint32_t idq = umma::idesc_bf16(128, NK, 0);
+    const uint32_t kbase = umma::smem_u32(sK0 + (t & 1) * (Sh::NP * PANEL));
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
+      umma::mma_bf16(tmem + Sh::TMEM_S + (t & 1) * NK, umma::sw128_desc(umma::smem_u32(sQ) + off, 16, 1024),
+                     umma::sw128_desc(kbase + off, 16, 1024), idq, kk > 0);
+    }
+    umma::commit(&bar_s);
+  };
+  auto issue_pv = [&](int t) {  // O += P_hi V(t) + P_lo V(t); one thread
+    constexpr uint32_t idp = umma::idesc_bf16(128, D, 1);
+    const uint32_t vbase = umma::smem_u32(sV0 + (t & 1) * (Sh::NP * PANEL));
+#pragma unroll
+    for (int kk = 0; kk < NK / 16; ++kk) {
+      const uint32_t aoff = (kk >> 2) * PANEL + (kk & 3) * 32;
+      const uint64_t bd = umma::sw128_desc(vbase + kk * 2048, PANEL, 1024);
+      umma::mma_bf16(tmem + Sh::TMEM_O, umma::sw128_desc(umma::smem_u32(sPH) + aoff, 16, 1024), bd, idp,
+                     t > 0 || kk > 0);
+      umma::mma_bf16(tmem + Sh::TMEM_O, umma::sw128_desc(umma::smem_u32(sPL) + aoff, 16, 1024), bd, idp, true);
+    }
+    umma::commit(&bar_o);
+  };
+
+  // ---- prologue: K and V of tile 0, K of tile 1, metadata of tile 0; S(0) ----
+  if (ntiles > 0) {
+    stage_rows(0, false);
+    stage_rows(0, true);
     umma::cp_async_commit();
+    if (ntiles > 1) stage_rows(1, false);
+    umma::cp_async_commit();
+    bool all_vis;
+    {
+      int pos;
+      float lg;
+      meta_begin(0, pos, lg);
+      all_vis = meta_end(0, pos, lg);
+    }
     umma::cp_async_wait_prior();
-    const uint8_t* sK = sK0 + (it & 1) * (Sh::NP * PANEL);
-    const uint8_t* sV = sV0 + (it & 1) * (Sh::NP * PANEL);
-    const int2* meta = meta0 + (it & 1) * NK;
     umma::fence_proxy_async_smem();
     umma::fence_before_sync();
-    __syncthreads();
-
-    // ---- 2. S = Q K^T ----
+    nomask_next = __syncthreads_and(all_vis);
     if (tid == 0) {
       umma::fence_after_sync();
-      constexpr uint32_t idq = umma::idesc_bf16(128, NK, 0);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
-        umma::mma_bf16(tmem + Sh::TMEM_S, umma::sw128_desc(umma::smem_u32(sQ) + off, 16, 1024),
-                       umma::sw128_desc(umma::smem_u32(sK) + off, 16, 1024), idq, kk > 0);
-      }
-      umma::commit(&bar_s);
+      issue_s(0);
     }
     ++n_s;
-    if (it + 1 < ntiles) stage_meta(it + 1);  // overlaps the S MMA
+  }
+
+  // Tile it: the tensor core runs S(it + 1) and P V(it - 1) .. P V(it) while the
+  // threads work on the softmax of tile it.
+  for (int it = 0; it < ntiles; ++it) {
+    const int bf = it & 1;
+    const bool nomask = nomask_next;  // every valid key of tile it is visible to every row
+    // (a) S(it) is done: S buffer bf can be read, K buffer bf is free again.
     {
       const bool ok = mbar_wait(&bar_s, w_s & 1);
       ++w_s;
@@ -243,23 +285,46 @@ __global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const Prefill
       }
       umma::fence_after_sync();
     }
+    // (b) prefetch K(it + 2) into K buffer bf; start loading the metadata of
+    // tile it + 1 (stored in (f)).
+    if (it + 2 < ntiles) stage_rows(it + 2, false);
+    umma::cp_async_commit();
+    int npos = INT_MAX;
+    float nlg = 0.f;
+    if (it + 1 < ntiles) meta_begin(it + 1, npos, nlg);
 
-    // ---- 3. softmax of this thread's row ----
+    // (c) softmax of this thread's row: both threads of a row load the whole
+    // row, mask it and find its max (the same decisions without talking); each
+    // turns its own 64 keys (P panel hh) into probabilities.
+    const int2* meta = meta0 + bf * NK;
     float s[NK];
 #pragma unroll
     for (int cb = 0; cb < NK / 32; ++cb) {
       float v[32];
-      umma::ld32(trow + Sh::TMEM_S + cb * 32, v);
+      umma::ld32(trow + Sh::TMEM_S + bf * NK + cb * 32, v);
 #pragma unroll
       for (int j = 0; j < 32; ++j) s[cb * 32 + j] = v[j];
     }
     float mt = -INFINITY;
+    if (nomask && row_ok) {
+      int k0, kn;
+      tile_keys(it, k0, kn);
 #pragma unroll
-    for (int j = 0; j < NK; ++j) {
-      const int2 mk = meta[j];
-      const bool vis = row_ok && mk.x <= tq && tq <= mk.y;
-      s[j] = vis ? s[j] * a.qscale : -INFINITY;
-      mt = fmaxf(mt, s[j]);
+      for (int j = 0; j < NK; j += 2) {
+        const float2 v = __fmul2_rn(make_float2(s[j], s[j + 1]), make_float2(a.qscale, a.qscale));
+        s[j] = j < kn ? v.x : -INFINITY;
+        s[j + 1] = j + 1 < kn ? v.y : -INFINITY;
+      }
+#pragma unroll
+      for (int j = 0; j < NK; j += 4) mt = fmaxf(mt, fmaxf(fmaxf(s[j], s[j + 1]), fmaxf(s[j + 2], s[j + 3])));
+    } else {
+#pragma unroll
+      for (int j = 0; j < NK; ++j) {
+        const int2 mk = meta[j];
+        const bool vis = row_ok && mk.x <= tq && tq <= mk.y;
+        s[j] = vis ? s[j] * a.qscale : -INFINITY;
+        mt = fmaxf(mt, s[j]);
+      }
     }
     bool rescale = false;
     float factor = 1.f;
@@ -273,29 +338,41 @@ __global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const Prefill
     }
     const float mref = m_run == -INFINITY ? 0.f : m_run;  // rows with nothing visible yet: p = 0
     float psum = 0.f;
+    uint32_t hi[NK / 16][4], lo[NK / 16][4];
 #pragma unroll
-    for (int q8 = 0; q8 < NK / 8; ++q8) {
-      uint32_t hi[4], lo[4];
+    for (int qq = 0; qq < NK / 16; ++qq) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float p0 = fast_exp2(s[q8 * 8 + 2 * e] - mref);
-        const float p1 = fast_exp2(s[q8 * 8 + 2 * e + 1] - mref);
+        const float p0 = fast_exp2((hh ? s[64 + qq * 8 + 2 * e] : s[qq * 8 + 2 * e]) - mref);
+        const float p1 = fast_exp2((hh ? s[64 + qq * 8 + 2 * e + 1] : s[qq * 8 + 2 * e + 1]) - mref);
         psum += p0 + p1;
         const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
         const float2 hf = __bfloat1622float2(h2);
         const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
-        hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
-        lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
+        hi[qq][e] = *reinterpret_cast<const uint32_t*>(&h2);
+        lo[qq][e] = *reinterpret_cast<const uint32_t*>(&l2);
       }
-      const int off = (q8 >> 3) * PANEL + r * 128 + (((q8 & 7) ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(sPH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(sPL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    l_run += psum;
-    // Rescale this warp's accumulator rows in tensor memory (warp-collective).
+
+    // (d) P V(it - 1) is done: the P buffers, O and V buffer bf ^ 1 are free.
+    if (w_o < n_o) {
+      const bool ok = mbar_wait(&bar_o, w_o & 1);
+      ++w_o;
+      if (__syncthreads_or(!ok)) {
+        failed = true;
+        break;
+      }
+      umma::fence_after_sync();
+    }
+    // (e) prefetch V(it + 1) into V buffer bf ^ 1.
+    if (it + 1 < ntiles) stage_rows(it + 1, true);
+    umma::cp_async_commit();
+    // (f) rescale this warp's accumulator rows (warp-collective; each half of the
+    // threads owns half of the output columns), then write P.
     if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-      for (int cb = 0; cb < D / 32; ++cb) {
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int cb = hh * (D / 64) + cc;
         float o[32];
         umma::ld32(trow + Sh::TMEM_O + cb * 32, o);
 #pragma unroll
@@ -303,24 +380,27 @@ __global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const Prefill
         umma::st32(trow + Sh::TMEM_O + cb * 32, o);
       }
     }
+#pragma unroll
+    for (int qq = 0; qq < NK / 16; ++qq) {
+      const int q8 = hh * (NK / 16) + qq;
+      const int off = (q8 >> 3) * PANEL + r * 128 + (((q8 & 7) ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(sPH + off) = make_uint4(hi[qq][0], hi[qq][1], hi[qq][2], hi[qq][3]);
+      *reinterpret_cast<uint4*>(sPL + off) = make_uint4(lo[qq][0], lo[qq][1], lo[qq][2], lo[qq][3]);
+    }
+    l_run += psum;
+    const bool nvis = it + 1 < ntiles ? meta_end(it + 1, npos, nlg) : true;
+    // (g) K(it + 1) and V(it) have landed (all groups but the two just committed).
+    umma::cp_async_wait_two();
     umma::fence_proxy_async_smem();
     umma::fence_before_sync();
-    __syncthreads();
-
-    // ---- 4. O += P_hi V + P_lo V ----
+    nomask_next = __syncthreads_and(nvis);
+    // (h) S(it + 1) first, so that the next softmax can start, then P V(it).
     if (tid == 0) {
       umma::fence_after_sync();
-      constexpr uint32_t idp = umma::idesc_bf16(128, D, 1);
-#pragma unroll
-      for (int kk = 0; kk < NK / 16; ++kk) {
-        const uint32_t aoff = (kk >> 2) * PANEL + (kk & 3) * 32;
-        const uint64_t bd = umma::sw128_desc(umma::smem_u32(sV) + kk * 2048, PANEL, 1024);
-        umma::mma_bf16(tmem + Sh::TMEM_O, umma::sw128_desc(umma::smem_u32(sPH) + aoff, 16, 1024), bd, idp,
-                       it > 0 || kk > 0);
-        umma::mma_bf16(tmem + Sh::TMEM_O, umma::sw128_desc(umma::smem_u32(sPL) + aoff, 16, 1024), bd, idp, true);
-      }
-      umma::commit(&bar_o);
+      if (it + 1 < ntiles) issue_s(it + 1);
+      issue_pv(it);
     }
+    if (it + 1 < ntiles) ++n_s;
     ++n_o;
   }
 
@@ -331,11 +411,17 @@ __global__ void __launch_bounds__(128, 1) prefill_attention_kernel(const Prefill
     umma::fence_after_sync();
   }
   if (!failed && ntiles > 0) {
-    // ---- epilogue: O / l -> out ----
-    const float inv = row_ok && l_run > 0.f ? 1.f / l_run : 0.f;
+    // ---- epilogue: O / l -> out; the row sum is the two halves' sums, swapped
+    // through shared memory that no MMA reads any more ----
+    float* lsw = reinterpret_cast<float*>(sPH);
+    lsw[hh * 128 + r] = l_run;
+    __syncthreads();
+    const float l_row = l_run + lsw[(1 - hh) * 128 + r];
+    const float inv = row_ok && l_row > 0.f ? 1.f / l_row : 0.f;
     float* orow = a.out + ((static_cast<size_t>(b) * Hq + h * G + rg) * a.C + rc) * D;
 #pragma unroll
-    for (int cb = 0; cb < D / 32; ++cb) {
+    for (int cc = 0; cc < D / 64; ++cc) {
+      const int cb = hh * (D / 64) + cc;
       float o[32];
       umma::ld32(trow + Sh::TMEM_O + cb * 32, o);
       if (row_ok) {
