@@ -146,6 +146,15 @@ int dms_cache_export_kv(dms_cache_t* cache, void* k_out, void* v_out, void* stre
  * DMS_ERR_CAPACITY or DMS_ERR_TIMEOUT) or DMS_ERR_CUDA if the stream failed. */
 int dms_cache_status(dms_cache_t* cache, void* stream);
 
+/* Failure-path self-test: enqueue one device-side wait, the same bounded wait
+ * the kernels use, on a barrier that nothing completes.  It gives up after the
+ * library's time limit (1.5 s) and latches DMS_ERR_TIMEOUT in the cache's
+ * error word, as a wait that ran out inside a kernel would; the next
+ * dms_cache_status() returns DMS_ERR_TIMEOUT and the cache should be destroyed.
+ * No fault or trap is involved; the GPU context stays usable.  (The method has
+ * no counterpart; this exists to test error reporting.) */
+int dms_cache_selftest_wait(dms_cache_t* cache, void* stream);
+
 /* Number of tokens appended so far (the host position counter t), or -1. */
 int64_t dms_cache_position(dms_cache_t* cache);
 

@@ -195,6 +195,22 @@ __global__ void __launch_bounds__(256) append_chunk_copy_kernel(CacheView c, con
   }
 }
 
+// Self-test of the device-side time limit: one warp waits, with the same
+// bounded wait the kernels use, on an mbarrier that nothing ever completes; the
+// wait gives up after its limit and the timeout is latched in the cache's error
+// word, as a real wait that ran out would.  Launched only by
+// dms_cache_selftest_wait.
+__global__ void wait_selftest_kernel(int32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(&bar, 0);
+  if (!ok && threadIdx.x == 0) atomicOr(err, kErrBitTimeout);
+}
+
 // Logical-order copy of the K and V pools (undoes the chunk permutation of K).
 // One thread per 16-byte chunk.
 template <int D>

@@ -437,6 +437,14 @@ int dms_cache_export_kv(dms_cache_t* c, void* k_out, void* v_out, void* stream) 
   return launch_status();
 }
 
+int dms_cache_selftest_wait(dms_cache_t* c, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  DeviceGuard g(c->device);
+  if (!g.ok) return DMS_ERR_CUDA;
+  dms::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(c->view.err);
+  return launch_status();
+}
+
 int dms_cache_status(dms_cache_t* c, void* stream) {
   if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
   DeviceGuard g(c->device);

@@ -40,6 +40,7 @@ SIGNATURES = {
     "dms_cache_slot_positions": (_I, [_P, _P, _P]),
     "dms_cache_export_kv": (_I, [_P, _P, _P, _P]),
     "dms_cache_status": (_I, [_P, _P]),
+    "dms_cache_selftest_wait": (_I, [_P, _P]),
     "dms_cache_position": (ctypes.c_int64, [_P]),
     "dms_error_string": (ctypes.c_char_p, [_I]),
     "dms_decode_attention_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, ctypes.c_float, _I, _P]),

@@ -321,3 +321,21 @@ def test_long_context_one_layer():
     chunked fill + 4 decode steps, all rows."""
     wl = W.WORKLOADS["long-context"]
     _prefill_then_decode(wl, wl.prefill, 4, rows=list(range(wl.B)), layer=3)
+
+
+def test_device_wait_time_limit_is_reported():
+    """A device-side wait that nothing completes gives up after its time limit
+    and surfaces as DMS_ERR_TIMEOUT; the context stays usable afterwards."""
+    lib = dms.load_library()
+    c = dms.DmsCache(1, 2, 16, 64, 16)
+    assert lib.dms_cache_selftest_wait(c.handle, torch.cuda.current_stream().cuda_stream) == dms.DMS_OK
+    assert c.status() == dms.DMS_ERR_TIMEOUT
+    assert c.status() == dms.DMS_ERR_TIMEOUT  # sticky
+    c.close()
+    # a fresh cache on the same context works
+    wl = _small("after-timeout", 1, 4, 2, 64, 16, 32, ("normal", 0.0, 1.0))
+    tr = Trajectory(wl, 20)
+    for _ in range(20):
+        tr.append()
+    q = W.q_range(wl, 0, 19, 20)[:, :, 0].contiguous()
+    tr.decode_and_compare(q, "after timeout")

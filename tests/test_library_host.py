@@ -48,6 +48,8 @@ def test_null_handle_rejected_without_device(lib):
     assert lib.dms_cache_slot_positions(None, None, None) == dms.DMS_ERR_BAD_HANDLE
     assert lib.dms_cache_export_kv(None, None, None, None) == dms.DMS_ERR_BAD_HANDLE
     assert lib.dms_cache_status(None, None) == dms.DMS_ERR_BAD_HANDLE
+    assert lib.dms_cache_selftest_wait(None, None) == dms.DMS_ERR_BAD_HANDLE
+    assert lib.dms_prefill(None, None, None, None, None, 4, None, 1.0, 4, None) == dms.DMS_ERR_BAD_HANDLE
     assert lib.dms_cache_position(None) == -1
     lib.dms_cache_destroy(None)  # ignored
     fake = ctypes.c_void_p(0x1000)  # never returned by dms_cache_create
