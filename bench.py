@@ -288,26 +288,30 @@ def time_device_leg(dms, cache, ins, warmup, steps, scale, device, clocks=None, 
 
 def time_e2e_leg(dms, W, wl, n0, warmup, steps, device, dist=None):
     """Same steps through the Python API with the step's inputs in pinned host
-    memory: every step copies q/k/v/logits host->device, runs append + decode,
-    copies the output device->host and waits for it."""
+    memory.  Every step copies its packed inputs (q | k | v | logits, one pinned
+    buffer) host->device in one copy, runs append + decode with one library call
+    (DmsCache.step -> dms_step), copies the output device->host and waits for it
+    before the next step starts."""
     cache = fill_cache(dms, W, wl, n0, device)
     ins = step_inputs(W, wl, n0, warmup + steps, device)
-    host = [[x.cpu().pin_memory() for x in lst] for lst in ins]
-    q_d = torch.empty_like(ins[0][0])
-    k_d = torch.empty_like(ins[1][0])
-    v_d = torch.empty_like(ins[2][0])
-    l_d = torch.empty_like(ins[3][0])
+    parts = [x[0] for x in ins]  # q, k, v, logits of one step (shapes and dtypes)
+    sizes = [t.numel() * t.element_size() for t in parts]
+    offs = [sum(sizes[:j]) for j in range(4)]
+    total = sum(sizes)
+    host = torch.empty((warmup + steps, total), dtype=torch.uint8).pin_memory()
+    for i in range(warmup + steps):
+        for j in range(4):
+            host[i, offs[j]:offs[j] + sizes[j]].copy_(ins[j][i].contiguous().view(-1).view(torch.uint8).cpu())
+    dev = torch.empty(total, dtype=torch.uint8, device=device)
+    views = [dev[offs[j]:offs[j] + sizes[j]].view(parts[j].dtype).view(parts[j].shape) for j in range(4)]
+    q_d, k_d, v_d, l_d = views
     out_d = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device=device)
     out_h = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32).pin_memory()
     stream = torch.cuda.current_stream(device)
 
     def step(i):
-        q_d.copy_(host[0][i], non_blocking=True)
-        k_d.copy_(host[1][i], non_blocking=True)
-        v_d.copy_(host[2][i], non_blocking=True)
-        l_d.copy_(host[3][i], non_blocking=True)
-        cache.append(k_d, v_d, l_d)
-        cache.decode_attention(q_d, out_d, wl.scale)
+        dev.copy_(host[i], non_blocking=True)
+        cache.step(k_d, v_d, l_d, q_d, out_d, wl.scale)
         out_h.copy_(out_d, non_blocking=True)
         stream.synchronize()
 
@@ -325,7 +329,7 @@ def time_e2e_leg(dms, W, wl, n0, warmup, steps, device, dist=None):
     t1.record(stream)
     torch.cuda.synchronize(device)
     ms = t0.elapsed_time(t1)
-    h2d = sum(x.numel() * x.element_size() for x in (q_d, k_d, v_d, l_d))
+    h2d = total
     d2h = out_h.numel() * out_h.element_size()
     assert bool(torch.isfinite(out_h).all())
     cache.close()
@@ -640,8 +644,8 @@ def main():
         ms, h2d, d2h = e2e
         line["e2e"] = {"value": job_tokens_per_s(wl.B, args.steps, world, ms), "unit": "tokens/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "note": "Python API, pinned host inputs copied in and output copied out every step, "
-                               "stream synchronized every step"}
+                       "note": "Python API (DmsCache.step = dms_step): each step's packed pinned inputs copied in "
+                               "(one copy), append + decode, output copied out, stream synchronized every step"}
     if not args.no_prefill and world == 1:
         line["prefill"] = time_prefill_leg(dms, W, args.prefill_chunks, device)
     if not args.no_cpu_baseline and world == 1:

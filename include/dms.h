@@ -130,6 +130,15 @@ int dms_prefill(dms_cache_t* cache, const void* q, const void* k, const void* v,
 int dms_decode_attention(dms_cache_t* cache, const void* q, float* out, float scale, int q_heads,
                          void* stream);
 
+/*
+ * One decode step in one call: dms_append(k, v, evict_logit) followed by
+ * dms_decode_attention(q, out, scale, q_heads), with the arguments checked once
+ * -- the same two kernels on `stream`, for callers that issue a step per layer
+ * per token and want one library crossing for it.
+ */
+int dms_step(dms_cache_t* cache, const void* k, const void* v, const float* evict_logit, const void* q, float* out,
+             float scale, int q_heads, void* stream);
+
 /* Copy the retained length of every (sequence, KV head) into out_dev
  * (int32 [batch][kv_heads], device memory), stream-ordered. */
 int dms_cache_lengths(dms_cache_t* cache, int32_t* out_dev, void* stream);

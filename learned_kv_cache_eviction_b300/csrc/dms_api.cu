@@ -401,6 +401,33 @@ int dms_decode_attention(dms_cache_t* c, const void* q, float* out, float scale,
   return c->D == 128 ? launch_decode_d<128>(c, q, out, scale, G, st) : launch_decode_d<64>(c, q, out, scale, G, st);
 }
 
+int dms_step(dms_cache_t* c, const void* k, const void* v, const float* evict_logit, const void* q, float* out,
+             float scale, int q_heads, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  if (!k || !v || !evict_logit || !q || !out || !aligned16(k) || !aligned16(v) || !aligned16(evict_logit) ||
+      !aligned16(q) || !aligned16(out) || q_heads < 1 || q_heads % c->H != 0 || q_heads / c->H > DMS_MAX_GROUP ||
+      !std::isfinite(scale))
+    return DMS_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return DMS_ERR_CUDA;
+  if (!device_pointer_ok(k, c->device) || !device_pointer_ok(v, c->device) ||
+      !device_pointer_ok(evict_logit, c->device) || !device_pointer_ok(q, c->device) ||
+      !device_pointer_ok(out, c->device))
+    return DMS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int blocks = (c->NH * 32 + 255) / 256;
+  const uint4* k4 = static_cast<const uint4*>(k);
+  const uint4* v4 = static_cast<const uint4*>(v);
+  int rc = c->D == 128 ? launch_pdl(dms::append_kernel<128>, dim3(blocks), dim3(256), 0, st, c->view, k4, v4,
+                                    evict_logit, c->t)
+                       : launch_pdl(dms::append_kernel<64>, dim3(blocks), dim3(256), 0, st, c->view, k4, v4,
+                                    evict_logit, c->t);
+  if (rc != DMS_OK) return rc;
+  c->t += 1;
+  const int G = q_heads / c->H;
+  return c->D == 128 ? launch_decode_d<128>(c, q, out, scale, G, st) : launch_decode_d<64>(c, q, out, scale, G, st);
+}
+
 int dms_cache_lengths(dms_cache_t* c, int32_t* out_dev, void* stream) {
   if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
   if (!out_dev) return DMS_ERR_INVALID_ARG;

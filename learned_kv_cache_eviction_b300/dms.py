@@ -36,6 +36,7 @@ SIGNATURES = {
     "dms_append_chunk": (_I, [_P, _P, _P, _P, _I, _P]),
     "dms_decode_attention": (_I, [_P, _P, _P, ctypes.c_float, _I, _P]),
     "dms_prefill": (_I, [_P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _P]),
+    "dms_step": (_I, [_P, _P, _P, _P, _P, _P, ctypes.c_float, _I, _P]),
     "dms_cache_lengths": (_I, [_P, _P, _P]),
     "dms_cache_slot_positions": (_I, [_P, _P, _P]),
     "dms_cache_export_kv": (_I, [_P, _P, _P, _P]),
@@ -174,6 +175,23 @@ class DmsCache:
         scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
         _check(self._lib.dms_prefill(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(), logits.data_ptr(), C,
                                      out.data_ptr(), scale, Hq, _stream_handle(stream)), "dms_prefill")
+        return out
+
+    def step(self, k: torch.Tensor, v: torch.Tensor, evict_logit: torch.Tensor, q: torch.Tensor,
+             out: torch.Tensor, scale: float | None = None, stream=None) -> torch.Tensor:
+        """Append one token and decode its query in one library call (dms_step).
+        k, v [B][Hkv][D] bf16, evict_logit [B][Hkv] fp32, q [B][Hq][D] bf16,
+        out [B][Hq][D] fp32 (preallocated)."""
+        B, H, D = self.batch, self.kv_heads, self.head_dim
+        Hq = q.shape[1] if q.dim() == 3 else -1
+        _need(k, "k", torch.bfloat16, (B, H, D), self.device)
+        _need(v, "v", torch.bfloat16, (B, H, D), self.device)
+        _need(evict_logit, "evict_logit", torch.float32, (B, H), self.device)
+        _need(q, "q", torch.bfloat16, (B, Hq, D), self.device)
+        _need(out, "out", torch.float32, (B, Hq, D), self.device)
+        scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+        _check(self._lib.dms_step(self.handle, k.data_ptr(), v.data_ptr(), evict_logit.data_ptr(), q.data_ptr(),
+                                  out.data_ptr(), scale, Hq, _stream_handle(stream)), "dms_step")
         return out
 
     def decode_attention(self, q: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,

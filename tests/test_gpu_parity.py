@@ -339,3 +339,26 @@ def test_device_wait_time_limit_is_reported():
         tr.append()
     q = W.q_range(wl, 0, 19, 20)[:, :, 0].contiguous()
     tr.decode_and_compare(q, "after timeout")
+
+
+def test_step_equals_append_then_decode():
+    """dms_step (one call) gives the same outputs and cache state, bit for bit,
+    as dms_append followed by dms_decode_attention."""
+    wl = _small("step", 2, 8, 2, 128, 16, 300, ("normal", 0.6, 1.0), seed=13)
+    T = 260
+    a = Trajectory(wl, T)
+    b = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
+    q = W.q_range(wl, 0, 0, T)
+    out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    for t in range(T):
+        k, v, lg = (a.k[:, :, t].contiguous().cuda(), a.v[:, :, t].contiguous().cuda(),
+                    a.lg[:, :, t].contiguous().cuda())
+        qt = q[:, :, t].contiguous().cuda()
+        a.cache.append(k, v, lg)
+        ref = a.cache.decode_attention(qt, scale=wl.scale)
+        b.step(k, v, lg, qt, out, scale=wl.scale)
+        if t % 37 == 0 or t == T - 1:
+            assert torch.equal(out, ref), t
+    assert torch.equal(a.cache.lengths(), b.lengths())
+    assert torch.equal(a.cache.slot_positions(), b.slot_positions())
+    assert b.position == T and b.status() == dms.DMS_OK
