@@ -407,6 +407,42 @@ def cpu_baseline(wl, n_ctx, seconds=12.0, rows=(0, 1)):
                       f"{wl.B} at positions {n_ctx - min(steps, 256)}..{n_ctx - 1} ({steps} steps, {dt:.1f} s)"}
 
 
+def time_variants(dms, W, device, steps):
+    """The ablation variants (eager eviction, windows 64 and 256, drifting CR)
+    at the headline shapes: each cache is filled to 16384 tokens, then `steps`
+    back-to-back dms_decode_attention calls are timed with events around the
+    pass.  Reported: time per launch, algorithmic GB/s and the realised CR."""
+    lib = dms.load_library()
+    stream = torch.cuda.current_stream(device)
+    rows = []
+    for name in ("qwen3-8b-eager", "qwen3-8b-w64", "qwen3-8b-w256", "qwen3-8b-drift"):
+        wl = W.WORKLOADS[name]
+        cache = fill_cache(dms, W, wl, wl.cap, device)
+        q = W.q_range(wl, 0, wl.cap - 1, wl.cap, device=device)[:, :, 0].contiguous()
+        out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device=device)
+        for _ in range(3):
+            lib.dms_decode_attention(cache.handle, q.data_ptr(), out.data_ptr(), wl.scale, wl.Hq, stream.cuda_stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            rc = lib.dms_decode_attention(cache.handle, q.data_ptr(), out.data_ptr(), wl.scale, wl.Hq,
+                                          stream.cuda_stream)
+            if rc:
+                raise dms.DmsError(rc, "dms_decode_attention")
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        us = e0.elapsed_time(e1) * 1e3 / steps
+        len_sum = int(cache.lengths().sum())
+        st = cache.status()
+        cache.close()
+        if st != dms.DMS_OK:
+            raise dms.DmsError(st, name)
+        rows.append({"workload": name, "window": wl.w, "context": wl.cap, "us_per_launch": us,
+                     "achieved_GBps": decode_bytes(wl, len_sum) / (us * 1e-6) / 1e9,
+                     "realised_cr": wl.B * wl.Hkv * wl.cap / len_sum, "note": wl.note})
+    return rows
+
+
 def measured_bf16_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -532,6 +568,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill leg and print its figures (for profiling)")
     ap.add_argument("--prefill-chunks", type=int, default=9)
@@ -646,6 +683,8 @@ def main():
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "note": "Python API (DmsCache.step = dms_step): each step's packed pinned inputs copied in "
                                "(one copy), append + decode, output copied out, stream synchronized every step"}
+    if not args.no_variants and world == 1:
+        line["variants"] = time_variants(dms, W, device, 32)
     if not args.no_prefill and world == 1:
         line["prefill"] = time_prefill_leg(dms, W, args.prefill_chunks, device)
     if not args.no_cpu_baseline and world == 1:

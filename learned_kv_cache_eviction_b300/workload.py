@@ -60,6 +60,7 @@ class Workload:
     cap: int
     seed: int
     logits: tuple  # ("normal", mu, sigma) | ("const", v) | ("beta_head",) | ("normal_forced_keep", mu, sigma, frac)
+                   # | ("drift", p_early, p_late, t_mid, t_width): eviction rate moving with position
     layers: int = 1
     prefill: int = 0  # tokens appended before decode (chunked)
     chunk: int = 512
@@ -115,6 +116,25 @@ WORKLOADS: dict[str, Workload] = {
         logits=("normal_forced_keep", 2.118, 1.5, 0.05), layers=8,
         prefill=32768, chunk=512, decode=4096,
         note="8 layers, 32K chunked prefill + 4K decode, 5% forced keep, CR 8"),
+    # Variants of the method's ablations and limitations, at the Qwen3-8B-like
+    # shapes: eager eviction (window 1), longer windows, and a compression ratio
+    # that drifts with sequence length (lighter before ~10K tokens, heavier after).
+    "qwen3-8b-eager": Workload(
+        "qwen3-8b-eager", B=32, Hq=32, Hkv=8, D=128, w=1, cap=16384, seed=2,
+        logits=("normal", 1.150, 1.0), prefill=1024, chunk=512, decode=15360,
+        note="eviction executed immediately (window 1), CR 8"),
+    "qwen3-8b-w64": Workload(
+        "qwen3-8b-w64", B=32, Hq=32, Hkv=8, D=128, w=64, cap=16384, seed=2,
+        logits=("normal", 1.150, 1.0), prefill=1024, chunk=512, decode=15360,
+        note="delay window 64, CR 8"),
+    "qwen3-8b-w256": Workload(
+        "qwen3-8b-w256", B=32, Hq=32, Hkv=8, D=128, w=256, cap=16384, seed=2,
+        logits=("normal", 1.150, 1.0), prefill=1024, chunk=512, decode=15360,
+        note="delay window 256, CR 8"),
+    "qwen3-8b-drift": Workload(
+        "qwen3-8b-drift", B=32, Hq=32, Hkv=8, D=128, w=16, cap=16384, seed=2,
+        logits=("drift", 0.75, 0.9375, 10000.0, 1000.0), prefill=1024, chunk=512, decode=15360,
+        note="eviction rate 75% (CR 4) early rising to 93.75% (CR 16) beyond ~10K tokens"),
     # Literal logit distributions of the benchmark plan (secondary rows: their
     # realised compression differs from the stated one).
     "llama-3.2-1b-literal": Workload(
@@ -167,6 +187,12 @@ def _row_block_kv(wl: Workload, layer: int, block: int, b: int, device):
         u = torch.rand((wl.Hkv, BLOCK), generator=_gen(device, wl.seed, layer, _KIND_FORCE, block, b),
                        device=device, dtype=torch.float32)
         lg = torch.where(u < float(wl.logits[3]), torch.full_like(lg, -10.0), lg)
+    elif kind == "drift":
+        p0, p1, t_mid, t_w = (float(x) for x in wl.logits[1:5])
+        pos = torch.arange(block * BLOCK, (block + 1) * BLOCK, dtype=torch.float64)
+        rate = p0 + (p1 - p0) * torch.sigmoid((pos - t_mid) / t_w)
+        mu = torch.special.ndtri(rate).to(device=device, dtype=torch.float32)  # P(N(mu, 1) > 0) = rate
+        lg = z + mu[None, :]
     else:
         raise ValueError(f"unknown logit distribution {kind!r}")
     return k, v, lg

@@ -362,3 +362,14 @@ def test_step_equals_append_then_decode():
     assert torch.equal(a.cache.lengths(), b.lengths())
     assert torch.equal(a.cache.slot_positions(), b.slot_positions())
     assert b.position == T and b.status() == dms.DMS_OK
+
+
+@pytest.mark.parametrize("name,T", [("qwen3-8b-eager", 3000), ("qwen3-8b-w64", 3000), ("qwen3-8b-w256", 3000),
+                                    ("qwen3-8b-drift", 11000)])
+def test_variant_workloads_sampled(name, T):
+    """The ablation variants at the Qwen3-8B-like head shapes (batch 4): eager
+    eviction (window 1), windows 64 and 256, and a compression ratio drifting
+    with length.  A T-token history filled in chunks, then 4 decode steps;
+    bookkeeping of all rows bit-exact, outputs of rows {0, 3}."""
+    wl = W.WORKLOADS[name].with_(B=4, cap=T + 4)
+    _prefill_then_decode(wl, T, 4, rows=[0, wl.B - 1])
