@@ -270,14 +270,27 @@ def _prefill_then_decode(wl, T_prefill, n_decode, rows, layer=0, check_kv=False)
 
 
 def test_llama_prefill_and_decode_sampled():
-    """Llama-3.2-1B-like: 3584-token chunked fill (C=512) + 512 decode steps;
-    bookkeeping every step, attention every 32nd step on rows {0, B-1}."""
+    """Llama-3.2-1B-like: 3584-token chunked prefill through dms_prefill (C=512,
+    attention checked on 4 positions of every chunk, rows {0, B-1}) + 512 decode
+    steps; bookkeeping every step, attention every 32nd step on rows {0, B-1}."""
     wl = W.WORKLOADS["llama-3.2-1b"]
     rows = [0, wl.B - 1]
     T0 = wl.prefill
     tr = Trajectory(wl, T0 + wl.decode, rows=rows)
     while tr.t < T0:
-        tr.append_chunk(min(wl.chunk, T0 - tr.t))
+        n = min(wl.chunk, T0 - tr.t)
+        t0 = tr.t
+        qc = W.q_range(wl, 0, t0, t0 + n)
+        sl = slice(t0, t0 + n)
+        out = tr.cache.prefill(qc.cuda(), tr.k[:, :, sl].contiguous().cuda(), tr.v[:, :, sl].contiguous().cuda(),
+                               tr.lg[:, :, sl].contiguous().cuda(), scale=wl.scale).cpu().numpy()
+        tr.sim.append_chunk(tr.e[:, :, sl])
+        tr.t += n
+        for c in (0, 1, n // 2, n - 1):
+            ref = O.decode_attention(qc[rows][:, :, c].float().numpy(), tr.k_np, tr.v_np, tr.e[rows], t0 + c,
+                                     wl.w, wl.scale)
+            assert_attention_close(out[rows][:, :, c], ref, f"{wl.name} prefill position {t0 + c}")
+        tr.check_lengths()
     q = W.q_range(wl, 0, T0, T0 + wl.decode)
     for j in range(wl.decode):
         tr.append()
