@@ -22,20 +22,19 @@ namespace dms {
 // entry records "no slot, keep", and the capacity error is latched).
 __device__ __forceinline__ int append_bookkeeping(const CacheView& c, int i, int64_t t, float logit,
                                                   int& len_reg) {
-  const int r = static_cast<int>(t % c.w);
-  int32_t* rs = c.ring_slot + static_cast<size_t>(i) * c.w;
-  uint8_t* rf = c.ring_flag + static_cast<size_t>(i) * c.w;
   int s;
-  if (t >= c.w && rf[r]) {
-    s = rs[r];  // token t - w leaves; token t takes its slot
+  const size_t old = t >= c.w ? ring_index(c.NH, c.w, i, t - c.w) : 0;
+  if (t >= c.w && c.ring_flag[old]) {
+    s = c.ring_slot[old];  // token t - w leaves; token t takes its slot
   } else if (len_reg < c.cap) {
     s = len_reg++;
   } else {
     s = -1;
     atomicOr(c.err, kErrBitCapacity);
   }
-  rs[r] = s;
-  rf[r] = (s >= 0 && logit > 0.0f) ? 1 : 0;
+  const size_t now = ring_index(c.NH, c.w, i, t);
+  c.ring_slot[now] = s;
+  c.ring_flag[now] = (s >= 0 && logit > 0.0f) ? 1 : 0;
   if (s >= 0) c.slot_pos[static_cast<size_t>(i) * c.cap + s] = static_cast<int32_t>(t);
   return s;
 }
@@ -55,9 +54,9 @@ __global__ void __launch_bounds__(256) append_kernel(CacheView c, const uint4* _
   if (i >= c.NH) return;
   int s = -1;
   if (lane == 0) {
-    int len_reg = c.len[i];
+    int len_reg = len_after(c, t)[i];
     s = append_bookkeeping(c, i, t, logit[i], len_reg);
-    c.len[i] = len_reg;
+    len_after(c, t + 1)[i] = len_reg;
   }
   s = __shfl_sync(0xffffffffu, s, 0);
   if (s < 0) return;
@@ -81,6 +80,8 @@ __global__ void __launch_bounds__(256) append_kernel(CacheView c, const uint4* _
 //   * For w <= 32 the state of the tokens before a batch comes from the
 //     previous batch's lanes by shuffles; for larger w, and for the first
 //     batch, from the ring in memory.
+//   * Lengths and ring are the double-buffered state of CacheView: read at
+//     t0, written at t0 + chunk.
 //   * Fresh slots are handed out in position order from len; beyond the
 //     capacity a token is dropped (ring entry "no slot, keep") and the
 //     capacity error is latched, as for a single append.
@@ -94,10 +95,8 @@ __global__ void __launch_bounds__(128) append_chunk_slots_kernel(CacheView c, co
   const int lane = threadIdx.x & 31;
   if (i >= c.NH) return;
   const int w = c.w;
-  int32_t* rs = c.ring_slot + static_cast<size_t>(i) * w;
-  uint8_t* rf = c.ring_flag + static_cast<size_t>(i) * w;
   int32_t* sp = c.slot_pos + static_cast<size_t>(i) * c.cap;
-  int len = c.len[i];
+  int len = len_after(c, t0)[i];
   bool overflow = false;
   int slot = -1, flag = 0;  // this lane's token in the current (then previous) batch
   for (int base = 0; base < chunk; base += 32) {
@@ -111,9 +110,9 @@ __global__ void __launch_bounds__(128) append_chunk_slots_kernel(CacheView c, co
       rslot = __shfl_sync(0xffffffffu, slot, (lane + 32 - w) & 31);
       rflag = __shfl_sync(0xffffffffu, flag, (lane + 32 - w) & 31);
     } else if (active && lane < w && t >= w) {
-      const int r = static_cast<int>(t % w);
-      rslot = rs[r];
-      rflag = rf[r];
+      const size_t e = ring_index(c.NH, w, i, t - w);
+      rslot = c.ring_slot[e];
+      rflag = c.ring_flag[e];
     }
     slot = -1;
     flag = 0;
@@ -145,17 +144,18 @@ __global__ void __launch_bounds__(128) append_chunk_slots_kernel(CacheView c, co
     const int nxt = __shfl_sync(0xffffffffu, slot, (lane + w) & 31);
     const bool superseded = w < 32 && lane + w < n && slot >= 0 && nxt == slot;
     if (active && slot >= 0 && !superseded) sp[slot] = static_cast<int32_t>(t);
-    // The ring keeps the last w tokens: each batch writes the entries of its
-    // lanes that no later lane of the batch overwrites.
-    if (active && lane + w >= n) {
-      const int r = static_cast<int>(t % w);
-      rs[r] = slot;
-      rf[r] = static_cast<uint8_t>(flag);
+    // The ring keeps the last 2w positions (two generations of w): each batch
+    // writes the entries of its lanes that no later lane of the batch (2w
+    // positions on, same entry) overwrites.
+    if (active && lane + 2 * w >= n) {
+      const size_t e = ring_index(c.NH, w, i, t);
+      c.ring_slot[e] = slot;
+      c.ring_flag[e] = static_cast<uint8_t>(flag);
     }
     __syncwarp();
   }
   if (lane == 0) {
-    c.len[i] = len;
+    len_after(c, t0 + chunk)[i] = len;
     if (overflow) atomicOr(c.err, kErrBitCapacity);
   }
 }
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(256) append_chunk_copy_kernel(CacheView c, con
   const int i = blockIdx.y;
   const int lane = threadIdx.x & 31;
   const int s0 = (static_cast<int>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * 32;
-  const int L = c.len[i];
+  const int L = len_after(c, t0 + chunk)[i];
   if (s0 >= L) return;
   const int s = s0 + lane;
   const int p = s < L ? c.slot_pos[static_cast<size_t>(i) * c.cap + s] : -1;

@@ -116,7 +116,7 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
   dms::DecodeArgs a;
   a.K = c->view.K;
   a.V = c->view.V;
-  a.len = c->view.len;
+  a.len = dms::len_after(c->view, c->t);
   a.q = static_cast<const uint16_t*>(q);
   a.out = out;
   a.part_acc = c->part_acc;
@@ -237,7 +237,7 @@ dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_di
   }
   const int64_t NH = static_cast<int64_t>(batch) * kv_heads;
   if (NH > (1 << 20) || NH * static_cast<int64_t>(capacity) >= (int64_t(1) << 31) ||
-      NH * static_cast<int64_t>(window) >= (int64_t(1) << 31)) {
+      2 * NH * static_cast<int64_t>(window) >= (int64_t(1) << 31)) {
     g_last_error = DMS_ERR_INVALID_ARG;
     return nullptr;
   }
@@ -263,7 +263,7 @@ dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_di
   }
   const size_t pool = static_cast<size_t>(NH) * capacity * head_dim * 2;
   const size_t nslot = static_cast<size_t>(NH) * capacity;
-  const size_t nring = static_cast<size_t>(NH) * window;
+  const size_t nring = 2 * static_cast<size_t>(NH) * window;  // two generations
   c->part_entries = static_cast<size_t>(c->num_sms) * dms::kMaxWarpsPerCta + NH;
   const size_t part_acc = c->part_entries * DMS_MAX_GROUP * head_dim * sizeof(float);
   const size_t part_ml = c->part_entries * DMS_MAX_GROUP * 2 * sizeof(float);
@@ -271,13 +271,13 @@ dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_di
             cudaMalloc(&c->view.slot_pos, nslot * 4) == cudaSuccess &&
             cudaMalloc(&c->view.ring_slot, nring * 4) == cudaSuccess &&
             cudaMalloc(&c->view.ring_flag, nring) == cudaSuccess &&
-            cudaMalloc(&c->view.len, NH * 4) == cudaSuccess && cudaMalloc(&c->view.err, kAlign) == cudaSuccess &&
+            cudaMalloc(&c->view.len, 2 * NH * 4) == cudaSuccess && cudaMalloc(&c->view.err, kAlign) == cudaSuccess &&
             cudaMalloc(&c->part_acc, part_acc) == cudaSuccess && cudaMalloc(&c->part_ml, part_ml) == cudaSuccess &&
             cudaMalloc(&c->head_cnt, NH * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->view.K, 0, pool) == cudaSuccess && cudaMemset(c->view.V, 0, pool) == cudaSuccess &&
        cudaMemset(c->view.slot_pos, 0xff, nslot * 4) == cudaSuccess &&
        cudaMemset(c->view.ring_slot, 0xff, nring * 4) == cudaSuccess &&
-       cudaMemset(c->view.ring_flag, 0, nring) == cudaSuccess && cudaMemset(c->view.len, 0, NH * 4) == cudaSuccess &&
+       cudaMemset(c->view.ring_flag, 0, nring) == cudaSuccess && cudaMemset(c->view.len, 0, 2 * NH * 4) == cudaSuccess &&
        cudaMemset(c->view.err, 0, kAlign) == cudaSuccess && cudaMemset(c->head_cnt, 0, NH * 4) == cudaSuccess &&
        cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
@@ -363,7 +363,7 @@ int dms_prefill(dms_cache_t* c, const void* q, const void* k, const void* v, con
   dms::PrefillArgs a;
   a.K = c->view.K;
   a.V = c->view.V;
-  a.len = c->view.len;
+  a.len = dms::len_after(c->view, c->t);
   a.slot_pos = c->view.slot_pos;
   a.ring_flag = c->view.ring_flag;
   a.q = static_cast<const uint4*>(q);
@@ -433,7 +433,7 @@ int dms_cache_lengths(dms_cache_t* c, int32_t* out_dev, void* stream) {
   if (!out_dev) return DMS_ERR_INVALID_ARG;
   DeviceGuard g(c->device);
   if (!device_pointer_ok(out_dev, c->device)) return DMS_ERR_INVALID_ARG;
-  return cudaMemcpyAsync(out_dev, c->view.len, static_cast<size_t>(c->NH) * 4, cudaMemcpyDeviceToDevice,
+  return cudaMemcpyAsync(out_dev, dms::len_after(c->view, c->t), static_cast<size_t>(c->NH) * 4, cudaMemcpyDeviceToDevice,
                          static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DMS_OK
              : DMS_ERR_CUDA;

@@ -19,16 +19,31 @@ constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;
 // 16-byte chunks of each row (chunk c of slot s lives at chunk c ^ (s & 7)),
 // so that a contiguous bulk copy of consecutive slots into shared memory can
 // be read one row per lane without bank conflicts.  V is stored unpermuted.
+//
+// The lengths and the ring are double-buffered, so that one kernel can read a
+// step's old state from every CTA while it writes the new state (the fused
+// append + decode step): the lengths after t appends are len[t & 1], and the
+// ring entry (slot, mark) of position p is ring[(p / w) & 1][i][p % w].
 struct CacheView {
   uint4* K;            // [NH][cap][D/8] 16-byte chunks (bf16 x 8)
   uint4* V;            // [NH][cap][D/8]
   int32_t* slot_pos;   // [NH][cap]
-  int32_t* ring_slot;  // [NH][w]
-  uint8_t* ring_flag;  // [NH][w]
-  int32_t* len;        // [NH]
+  int32_t* ring_slot;  // [2][NH][w]
+  uint8_t* ring_flag;  // [2][NH][w]
+  int32_t* len;        // [2][NH]
   int32_t* err;        // sticky error bits
   int NH, cap, D, w;
 };
+
+// Lengths after t appends.
+__host__ __device__ __forceinline__ int32_t* len_after(const CacheView& c, int64_t t) {
+  return c.len + (t & 1) * static_cast<int64_t>(c.NH);
+}
+
+// Index of the ring entry of position p of head i.
+__host__ __device__ __forceinline__ size_t ring_index(int NH, int w, int i, int64_t p) {
+  return (static_cast<size_t>((p / w) & 1) * NH + i) * w + static_cast<size_t>(p % w);
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -75,9 +75,9 @@ struct PrefillShape {
 struct PrefillArgs {
   const uint4* K;            // cache K pool [NH][cap][D/8] (chunk-permuted rows)
   const uint4* V;            // cache V pool [NH][cap][D/8]
-  const int32_t* len;        // [NH] retained lengths before the chunk
+  const int32_t* len;        // [NH] retained lengths before the chunk (the current buffer)
   const int32_t* slot_pos;   // [NH][cap]
-  const uint8_t* ring_flag;  // [NH][w]
+  const uint8_t* ring_flag;  // [2][NH][w], entry of position p at ring_index(NH, w, i, p)
   const uint4* q;            // bf16 [B][Hq][C][D]
   const uint4* kc;           // bf16 [B][Hkv][C][D], the chunk's keys
   const uint4* vc;           // bf16 [B][Hkv][C][D]
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(256, 1) prefill_attention_kernel(const Prefill
     int last = -1;  // invisible unless set below
     if (pos != INT_MAX) {
       const bool marked = from_cache
-                              ? (pos >= pend_lo && a.ring_flag[static_cast<size_t>(i) * a.w + pos % a.w] != 0)
+                              ? (pos >= pend_lo && a.ring_flag[ring_index(a.NH, a.w, i, pos)] != 0)
                               : lg > 0.0f;
       last = marked ? pos + a.w - 1 : INT_MAX;
     }
