@@ -38,7 +38,7 @@ if ROOT not in sys.path:
 METRIC = "decode-attn tokens/s and achieved HBM GB/s (% of peak) at CR 8, Qwen3-8B shapes"
 NOMINAL_HBM_GBS = 8000.0  # "roughly 8 TB/s" stated with the target
 FALLBACK_HBM_GBS = 6400.0
-PROFILE_FILE = os.path.join(ROOT, "profiles", "decode_kernel_qwen3-8b_cr8_n16384.md")
+PROFILE_FILE = os.path.join(ROOT, "profiles", "decode_kernel_fused_step_qwen3-8b_cr8_n16384.md")
 KERNEL_SOURCES = ["decode.cuh", "dms_device.cuh"]
 
 
@@ -210,15 +210,16 @@ def step_inputs(W, wl, t0, n, device, layer=0):
 
 def time_device_leg(dms, cache, ins, warmup, steps, scale, device, clocks=None, dist=None):
     """Warm-up, then three passes through the C ABI on device-resident inputs.
-    Pass A (the headline): ``steps`` steps (append + decode), events only
-    around the whole pass, so consecutive kernels keep their programmatic-launch
-    overlap.  Pass B: ``steps`` more steps with events around every
-    dms_decode_attention call; the events break the launch overlap, so these
-    per-call times carry a launch gap each.  Pass C (the decode kernel's
-    roofline): ``steps`` back-to-back dms_decode_attention calls on the final
-    cache state, events around the whole pass -- the kernel's average
-    in-stream duration.  The retained K/V (> 126 MB L2) is re-read from HBM by
-    every call."""
+    Pass A (the headline): ``steps`` calls of dms_step (append + decode in one
+    launch of the fused decode kernel), events only around the whole pass, so
+    consecutive launches keep their programmatic-launch overlap; the pass's
+    mean is that kernel's in-stream duration.  Pass B: ``steps`` more steps as
+    dms_append + dms_decode_attention with events around every decode call;
+    the events break the launch overlap, so these per-call times carry a
+    launch gap each.  Pass C: ``steps`` back-to-back dms_decode_attention
+    calls on the final cache state, events around the whole pass -- the plain
+    decode kernel's average in-stream duration.  The retained K/V (> 126 MB
+    L2) is re-read from HBM by every call."""
     lib = dms.load_library()
     h = cache.handle
     stream = torch.cuda.current_stream(device)
@@ -238,9 +239,14 @@ def time_device_leg(dms, cache, ins, warmup, steps, scale, device, clocks=None, 
         if rc:
             raise dms.DmsError(rc, "dms_decode_attention")
 
+    def step(i):
+        rc = lib.dms_step(h, ks[i].data_ptr(), vs[i].data_ptr(), ls[i].data_ptr(), qs[i].data_ptr(), outp, scale,
+                          Hq, sh)
+        if rc:
+            raise dms.DmsError(rc, "dms_step")
+
     for i in range(warmup):
-        append(i)
-        decode(i)
+        step(i)
     torch.cuda.synchronize(device)
     len0 = int(cache.lengths().sum())
     if dist is not None:
@@ -251,8 +257,7 @@ def time_device_leg(dms, cache, ins, warmup, steps, scale, device, clocks=None, 
     with (clocks if clocks is not None else _Null()):
         t_start.record(stream)
         for i in range(warmup, warmup + steps):
-            append(i)
-            decode(i)
+            step(i)
         t_stop.record(stream)
         torch.cuda.synchronize(device)
     if dist is not None:
@@ -360,6 +365,14 @@ def decode_bytes(wl, len_sum):
     """Algorithmic bytes of one decode call: retained K and V (bf16), q (bf16),
     out (fp32) and the lengths (int32)."""
     return len_sum * 2 * wl.D * 2 + wl.B * wl.Hq * wl.D * (2 + 4) + wl.B * wl.Hkv * 4
+
+
+def append_bytes(wl):
+    """Algorithmic bytes of appending one token to every head: the new K and V
+    rows read and written (bf16), its logit (fp32), the new length (int32), the
+    ring entries of t - w read and of t written (slot int32 + mark byte) and its
+    slot-map entry (int32)."""
+    return wl.B * wl.Hkv * (4 * wl.D * 2 + 4 + 4 + 2 * 5 + 4)
 
 
 # ---------------------------------------------------------------------------
@@ -640,8 +653,12 @@ def main():
         return
 
     len_avg = 0.5 * (r["len_sum_start"] + r["len_sum_end"])
-    alg = decode_bytes(wl, r["len_sum_c"])
-    achieved = alg / (r["decode_us"] * 1e-6) / 1e9
+    # the fused kernel of pass A: decode over the lengths after each step's
+    # append (their mean over the pass) plus the append itself
+    step_us = total_ms * 1e3 / args.steps
+    alg = decode_bytes(wl, len_avg) + append_bytes(wl)
+    achieved = alg / (step_us * 1e-6) / 1e9
+    dec_bytes_c = decode_bytes(wl, r["len_sum_c"])
     peak, peak_kind = measured_hbm_peak()
     value = job_tokens_per_s(wl.B, args.steps, world, total_ms)
     ctx_avg = n_end - 1.5 * args.steps
@@ -653,19 +670,21 @@ def main():
         "config": workload_config(wl, n_end),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} HBM copy bandwidth", "traffic": profiled_traffic(),
-                     "kernel": "decode_kernel (one launch per dms_decode_attention call)",
-                     "algorithmic_bytes_per_launch": alg, "us_per_launch": r["decode_us"],
-                     "us_source": "mean of back-to-back dms_decode_attention calls (events around the pass)",
+                     "kernel": "decode_kernel<128, 4, fused> (append + decode, one launch per dms_step)",
+                     "algorithmic_bytes_per_launch": alg, "us_per_launch": step_us,
+                     "us_source": "mean of the timed dms_step calls (events around the pass)",
                      "frac_of_nominal_8TBps": achieved / NOMINAL_HBM_GBS},
         "decode_attention": {"us_per_launch_back_to_back": r["decode_us"],
+                             "achieved_GBps": dec_bytes_c / (r["decode_us"] * 1e-6) / 1e9,
+                             "frac": dec_bytes_c / (r["decode_us"] * 1e-6) / 1e9 / peak,
                              "us_per_call_events_mean": r["decode_us_call"],
                              "us_per_call_events_median": r["decode_us_call_median"],
                              "note": "per-call events sit between launches and add a launch gap to each call",
                              "tokens_per_s": wl.B / (r["decode_us"] * 1e-6),
                              "kv_token_reads_per_step": len_avg,
                              "realised_cr": wl.B * wl.Hkv * ctx_avg / len_avg},
-        "gpu_launches": 2 * args.steps,
-        "gpu_launches_note": "per timed step: append_kernel + decode_kernel",
+        "gpu_launches": args.steps,
+        "gpu_launches_note": "per timed step: one decode_kernel launch (fused append + decode)",
         "clocks": clocks.summary(),
     }
     if cr1 is not None:

@@ -59,7 +59,13 @@ struct DecodeShape {
   static constexpr int QV = (G * D / 8 + 31) / 32;  // 16-byte q chunks per lane
   static constexpr int OFF_P = OFF_QS + ((G * QROW * 4 + 15) / 16) * 16;
   static constexpr int OFF_BAR = OFF_P + TK * PROW * 4;
-  static constexpr int WARP_BYTES = ((OFF_BAR + NST * 8 + 127) / 128) * 128;
+  // Fused step: per-warp state kept in shared memory rather than in registers
+  // (the decode loop has none to spare): the new token's slots of the first
+  // FX_HEADS heads of the warp's range, the first head, the current segment's.
+  static constexpr int FX_HEADS = 14;
+  static constexpr int FX_I0 = FX_HEADS, FX_SEG = FX_HEADS + 1;
+  static constexpr int OFF_FX = OFF_BAR + NST * 8;
+  static constexpr int WARP_BYTES = ((OFF_FX + (FX_HEADS + 2) * 4 + 127) / 128) * 128;
   static constexpr int kSmemBudget = 227 * 1024 - 1024;  // leaves room for static shared memory
   // Warps per CTA: 12 (three per scheduler) where the shared memory allows.  With
   // three warps on a scheduler its register file leaves 168 registers per thread;
@@ -91,7 +97,68 @@ struct DecodeArgs {
   int32_t* err;
   int NH, Hkv, cap;
   float qscale;  // scale * log2(e)
+  // Fused step only (decode_kernel<D, G, true>, dms_step): the new token of
+  // position t is appended in the same launch.  `len` then holds the lengths
+  // before it; the kernel decodes over the lengths after it and writes those,
+  // the token's ring entry, slot map entry and K/V row into the other halves
+  // of the double-buffered state (see CacheView), which no CTA reads.
+  const uint4* k_new;     // [NH][D/8] the new token's K and V
+  const uint4* v_new;
+  const float* logit_new;  // [NH]
+  uint4* K_w;             // the K and V pools, writable
+  uint4* V_w;
+  int32_t* slot_pos;      // [NH][cap]
+  int32_t* ring_slot;     // [2][NH][w]
+  uint8_t* ring_flag;     // [2][NH][w]
+  int32_t* len_new;       // [NH] lengths after the append
+  int64_t t;
+  int w;
 };
+
+// The new token's slot in head x for the fused step: the slot of token t - w if
+// that token was stored and marked (it leaves now), else the next free slot,
+// else -1 (capacity exceeded).  Reads only the state before the step.
+__device__ __forceinline__ int fused_new_slot(const DecodeArgs& a, int x, int L_old) {
+  if (a.t >= a.w) {
+    const size_t e = ring_index(a.NH, a.w, x, a.t - a.w);
+    if (a.ring_flag[e]) return a.ring_slot[e];
+  }
+  return L_old < a.cap ? L_old : -1;
+}
+
+// Not inlined: the slot lookup of a head beyond the first 32 of a warp's range
+// (rare), kept out of the decode loop's code.
+static __device__ __noinline__ int fused_new_slot_far(const DecodeArgs& a, int x) {
+  return fused_new_slot(a, x, a.len[x]);
+}
+
+// Fused step, not inlined (once per head, in the warp whose tile holds the new
+// token's slot): overwrite row j of the staged tile with the new token's K row
+// (at the pool's chunk order for slot s_new) and V row from the step's input.
+// The tile's copy of that pool row is discarded: the row is being written in
+// the same launch.  The proxy fence orders these stores before the bulk copy
+// that next refills the buffer.
+static __device__ __noinline__ void patch_new_row(const DecodeArgs& a, uint4* Kt, uint4* Vt, int i, int j, int s_new,
+                                                  int CH, int lane) {
+  if (lane < CH) {
+    Kt[j * CH + (lane ^ (s_new & 7))] = __ldg(a.k_new + static_cast<size_t>(i) * CH + lane);
+  } else if (lane < 2 * CH) {
+    Vt[j * CH + lane - CH] = __ldg(a.v_new + static_cast<size_t>(i) * CH + lane - CH);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+}
+
+// Retained length of head x as this launch decodes it.
+template <bool FUSED>
+__device__ __forceinline__ int decode_len(const DecodeArgs& a, int x) {
+  const int L = a.len[x];
+  if constexpr (FUSED) {
+    const bool retire = a.t >= a.w && a.ring_flag[ring_index(a.NH, a.w, x, a.t - a.w)] != 0;
+    return (!retire && L < a.cap) ? L + 1 : L;
+  }
+  return L;
+}
 
 // Retained-slot iterator over one warp's global range [A, E).
 struct TileIter {
@@ -104,24 +171,26 @@ struct TileIter {
   bool valid;
   bool first;  // next tile opens a new segment (head)
 
-  __device__ __forceinline__ void start(const int32_t* len, int i0, int64_t P0, int64_t A, int64_t E_) {
+  template <typename LenF>
+  __device__ __forceinline__ void start(const LenF& len, int i0, int64_t P0, int64_t A, int64_t E_) {
     i = i0;
     P = P0;
     E = E_;
-    L = len[i0];
+    L = len(i0);
     s = static_cast<int>(A - P0);
     send = static_cast<int>(min(E, P0 + L) - P0);
     valid = s < send;
     first = true;
   }
-  __device__ __forceinline__ void advance(const int32_t* len, int NH, int cnt) {
+  template <typename LenF>
+  __device__ __forceinline__ void advance(const LenF& len, int NH, int cnt) {
     s += cnt;
     first = false;
     if (s < send) return;
     P += L;
     ++i;
     while (P < E && i < NH) {
-      L = len[i];
+      L = len(i);
       if (L > 0) break;
       ++i;
     }
@@ -137,10 +206,11 @@ struct TileIter {
 
 // Exclusive prefix sums of len[0..NH) into pre[0..NH] (shared memory) by the
 // whole CTA, reading each length from global memory once.
-__device__ __forceinline__ void scan_lengths(const int32_t* __restrict__ len, int NH, int* pre) {
+template <typename LenF>
+__device__ __forceinline__ void scan_lengths(const LenF& len, int NH, int* pre) {
   __shared__ int wsum[32];
   const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  for (int x = tid; x < NH; x += nt) pre[x] = len[x];
+  for (int x = tid; x < NH; x += nt) pre[x] = len(x);
   __syncthreads();
   const int per = (NH + nt - 1) / nt;
   const int b0 = min(NH, tid * per), b1 = min(NH, b0 + per);
@@ -259,7 +329,7 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, size_t base,
   }
 }
 
-template <int D, int G>
+template <int D, int G, bool FUSED>
 __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(const DecodeArgs a) {
   using Sh = DecodeShape<D, G>;
   constexpr int NW = Sh::NW, TK = Sh::TK, NST = Sh::NST, CH = Sh::CH, HCH = Sh::HCH, EL = Sh::EL;
@@ -272,14 +342,74 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
   griddep_launch_dependents();
 
   // ---- prologue: prefix sums of the retained lengths, warp ranges ----
-  int* pre = reinterpret_cast<int*>(smem);  // aliases the warp regions until the barrier below
-  scan_lengths(a.len, a.NH, pre);
-  const int64_t S = pre[a.NH];
   const int wl = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int64_t Pe = static_cast<int64_t>(gridDim.x) * NW;
+  const int64_t wg = static_cast<int64_t>(blockIdx.x) * NW + wl;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * NW;
+  auto lenf = [&](int x) { return decode_len<FUSED>(a, x); };
+  int* pre = reinterpret_cast<int*>(smem);  // [NH + 1]; aliases the warp regions until the barrier below
+  int* sn = pre + a.NH + 1;                 // fused step: [NH] the new token's slot in each head
+  // Fused step: warp x of the grid appends the token to head x (and x + nwarps,
+  // ...).  Its row chunk (K for lanes < CH, V for lanes CH .. 2 CH - 1) and
+  // logit are loaded now, in flight during the scan.
+  uint4 own_row = make_uint4(0u, 0u, 0u, 0u);
+  float own_logit = 0.f;
+  if constexpr (FUSED) {
+    if (wg < a.NH) {
+      if (lane < 2 * CH)
+        own_row = __ldg((lane < CH ? a.k_new : a.v_new) + static_cast<size_t>(wg) * CH + (lane % CH));
+      own_logit = __ldg(a.logit_new + wg);
+    }
+  }
+  // The scan reads each head's length (and, fused, the ring entry of t - w) once;
+  // the fused scan also records the new token's slot in sn.
+  auto scanf = [&](int x) {
+    if constexpr (FUSED) {
+      const int L = a.len[x];
+      int fl = 0, sl = 0;
+      if (a.t >= a.w) {
+        const size_t e = ring_index(a.NH, a.w, x, a.t - a.w);
+        fl = a.ring_flag[e];
+        sl = a.ring_slot[e];
+      }
+      sn[x] = fl ? sl : (L < a.cap ? L : -1);
+      return (fl || L >= a.cap) ? L : L + 1;
+    } else {
+      return a.len[x];
+    }
+  };
+  scan_lengths(scanf, a.NH, pre);
+  if constexpr (FUSED) {
+    // Bookkeeping and row of the new token; none of it is read by this launch
+    // (other halves of the double-buffered state, the slot map, and a pool row
+    // that every tile copy skips: the new row is copied from the input).
+    for (int64_t x = wg; x < a.NH; x += nwarps) {
+      const int i = static_cast<int>(x);
+      const int s_new = sn[i];
+      uint4 rowc = own_row;
+      float lg = own_logit;
+      if (x != wg) {
+        if (lane < 2 * CH) rowc = __ldg((lane < CH ? a.k_new : a.v_new) + static_cast<size_t>(i) * CH + (lane % CH));
+        lg = __ldg(a.logit_new + i);
+      }
+      if (lane == 0) {
+        a.len_new[i] = pre[i + 1] - pre[i];
+        const size_t e = ring_index(a.NH, a.w, i, a.t);
+        a.ring_slot[e] = s_new;
+        a.ring_flag[e] = (s_new >= 0 && lg > 0.0f) ? 1 : 0;
+        if (s_new >= 0) a.slot_pos[static_cast<size_t>(i) * a.cap + s_new] = static_cast<int32_t>(a.t);
+        else atomicOr(a.err, kErrBitCapacity);
+      }
+      if (s_new >= 0) {
+        const size_t row = (static_cast<size_t>(i) * a.cap + s_new) * CH;
+        if (lane < CH) a.K_w[row + (lane ^ (s_new & 7))] = rowc;
+        else if (lane < 2 * CH) a.V_w[row + lane - CH] = rowc;
+      }
+    }
+  }
+  const int64_t S = pre[a.NH];
+  int64_t Pe = nwarps;
   if (S / kMinSlotsPerWarp < Pe) Pe = S / kMinSlotsPerWarp;
   if (Pe < 1) Pe = 1;
-  const int64_t wg = static_cast<int64_t>(blockIdx.x) * NW + wl;
   const bool active = S > 0 && wg < Pe;
   int64_t A = 0, E = 0, P0 = 0;
   int i0 = 0;
@@ -294,7 +424,14 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
     i0 = lo;
     P0 = pre[lo];
   }
+  // Fused step: the new token's slots of heads i0, i0 + 1, ... (read before the
+  // barrier, which ends the prefix sums' lease on the warp regions).
+  int snl = -1;
+  if constexpr (FUSED) {
+    if (active && lane < Sh::FX_HEADS && i0 + lane < a.NH) snl = sn[i0 + lane];
+  }
   __syncthreads();
+
   if (!active) return;
 
   // ---- per-warp shared memory ----
@@ -304,15 +441,23 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
   float* qs = reinterpret_cast<float*>(wbase + Sh::OFF_QS);
   float* pb = reinterpret_cast<float*>(wbase + Sh::OFF_P);
   uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + Sh::OFF_BAR);  // [NST] tiles
+  int* fx = reinterpret_cast<int*>(wbase + Sh::OFF_FX);               // fused-step state
   if (lane == 0) {
     for (int x = 0; x < NST; ++x) mbar_init(&bars[x], 1);
     fence_barrier_init();
+  }
+  if constexpr (FUSED) {
+    if (lane < Sh::FX_HEADS) fx[lane] = snl;
+    if (lane == 0) {
+      fx[Sh::FX_I0] = i0;
+      fx[Sh::FX_SEG] = -1;
+    }
   }
   __syncwarp();
 
   const int Hq = a.Hkv * G;
   TileIter is, cs;
-  is.start(a.len, i0, P0, A, E);
+  is.start(lenf, i0, P0, A, E);
   cs = is;
   int n_issued = 0, n_cons = 0, nq_issued = 0, nq_conv = 0;
   constexpr int QV = Sh::QV;
@@ -344,7 +489,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
         ++nq_issued;
       }
       ++n_issued;
-      is.advance(a.len, a.NH, cnt);
+      is.advance(lenf, a.NH, cnt);
     }
   };
 
@@ -392,6 +537,13 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
       seg_i = cs.i;
       seg_L = cs.L;
       seg_P = cs.P;
+      if constexpr (FUSED) {
+        const int d = cs.i - fx[Sh::FX_I0];
+        const int sw = d < Sh::FX_HEADS ? fx[d] : fused_new_slot_far(a, cs.i);
+        __syncwarp();
+        if (lane == 0) fx[Sh::FX_SEG] = sw;
+        __syncwarp();
+      }
       try_issue();
     }
 
@@ -401,6 +553,13 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
     if (n_issued <= n_cons || !mbar_wait(&bars[buf], (n_cons / NST) & 1)) {
       fail_and_drain();
       return;
+    }
+
+    if constexpr (FUSED) {
+      const int sw = fx[Sh::FX_SEG];  // reloaded after the wait (the wait clobbers memory)
+      if (static_cast<unsigned>(sw - s0) < static_cast<unsigned>(cnt))
+        patch_new_row(a, reinterpret_cast<uint4*>(Ks + buf * TILEB), reinterpret_cast<uint4*>(Vs + buf * TILEB),
+                      seg_i, sw - s0, sw, CH, lane);
     }
 
     // ---- QK: lanes r and r + 16 score slot s0 + r over the two halves of D ----
@@ -507,7 +666,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
     __syncwarp();
     ++n_cons;
     const int cur_i = cs.i;
-    cs.advance(a.len, a.NH, cnt);
+    cs.advance(lenf, a.NH, cnt);
     const bool seg_end = !cs.valid || cs.i != cur_i;
 
     if (seg_end) {

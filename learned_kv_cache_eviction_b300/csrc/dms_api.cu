@@ -97,23 +97,35 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
   return launch_status();
 }
 
-template <int D, int G>
-int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaStream_t st) {
+// The new token of a fused step (dms_step): its K, V rows and eviction logit.
+struct StepInput {
+  const uint4* k;
+  const uint4* v;
+  const float* logit;
+};
+
+// Decode launch.  Plain (FUSED false): attention of q over the cache as it
+// stands at position c->t.  Fused (FUSED true, `in` set): the token of
+// position c->t is appended in the same launch and the attention runs over
+// the cache after it; the caller then advances c->t.
+template <int D, int G, bool FUSED>
+int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaStream_t st, const StepInput* in) {
   using Sh = dms::DecodeShape<D, G>;
   static bool attr_done[64] = {};
   if (c->device < 64 && !attr_done[c->device]) {
-    if (cudaFuncSetAttribute(dms::decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(dms::decode_kernel<D, G, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Sh::SMEM) != cudaSuccess)
       return DMS_ERR_CUDA;
     attr_done[c->device] = true;
   }
-  if (static_cast<int64_t>(c->NH + 1) * 4 > Sh::SMEM) return DMS_ERR_INVALID_ARG;
+  // The prologue's prefix sums (and, fused, each head's new slot) fit in shared memory.
+  if (static_cast<int64_t>((FUSED ? 2 : 1) * c->NH + 1) * 4 > Sh::SMEM) return DMS_ERR_INVALID_ARG;
   // Upper bound of the retained slots (the exact sum lives on the device).
-  const int64_t smax = static_cast<int64_t>(c->NH) * std::min<int64_t>(c->t, c->cap);
+  const int64_t smax = static_cast<int64_t>(c->NH) * std::min<int64_t>(c->t + (FUSED ? 1 : 0), c->cap);
   const int64_t want = (smax + int64_t(dms::kMinSlotsPerWarp) * Sh::NW - 1) / (int64_t(dms::kMinSlotsPerWarp) * Sh::NW);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(c->num_sms, want)));
   if (static_cast<size_t>(grid) * Sh::NW + c->NH > c->part_entries) return DMS_ERR_INVALID_ARG;
-  dms::DecodeArgs a;
+  dms::DecodeArgs a{};
   a.K = c->view.K;
   a.V = c->view.V;
   a.len = dms::len_after(c->view, c->t);
@@ -127,20 +139,41 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
   a.Hkv = c->H;
   a.cap = c->cap;
   a.qscale = scale * 1.4426950408889634f;  // log2(e): softmax evaluated as 2^(x log2 e)
-  return launch_pdl(dms::decode_kernel<D, G>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
+  a.k_new = nullptr;
+  a.v_new = nullptr;
+  a.logit_new = nullptr;
+  a.K_w = nullptr;
+  a.V_w = nullptr;
+  a.slot_pos = nullptr;
+  a.ring_slot = c->view.ring_slot;
+  a.ring_flag = c->view.ring_flag;
+  a.len_new = nullptr;
+  a.t = c->t;
+  a.w = c->w;
+  if constexpr (FUSED) {
+    a.k_new = in->k;
+    a.v_new = in->v;
+    a.logit_new = in->logit;
+    a.K_w = c->view.K;
+    a.V_w = c->view.V;
+    a.slot_pos = c->view.slot_pos;
+    a.len_new = dms::len_after(c->view, c->t + 1);
+  }
+  return launch_pdl(dms::decode_kernel<D, G, FUSED>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
 }
 
-template <int D>
-int launch_decode_d(dms_cache* c, const void* q, float* out, float scale, int G, cudaStream_t st) {
+template <int D, bool FUSED>
+int launch_decode_d(dms_cache* c, const void* q, float* out, float scale, int G, cudaStream_t st,
+                    const StepInput* in = nullptr) {
   switch (G) {
-    case 1: return launch_decode_t<D, 1>(c, q, out, scale, st);
-    case 2: return launch_decode_t<D, 2>(c, q, out, scale, st);
-    case 3: return launch_decode_t<D, 3>(c, q, out, scale, st);
-    case 4: return launch_decode_t<D, 4>(c, q, out, scale, st);
-    case 5: return launch_decode_t<D, 5>(c, q, out, scale, st);
-    case 6: return launch_decode_t<D, 6>(c, q, out, scale, st);
-    case 7: return launch_decode_t<D, 7>(c, q, out, scale, st);
-    case 8: return launch_decode_t<D, 8>(c, q, out, scale, st);
+    case 1: return launch_decode_t<D, 1, FUSED>(c, q, out, scale, st, in);
+    case 2: return launch_decode_t<D, 2, FUSED>(c, q, out, scale, st, in);
+    case 3: return launch_decode_t<D, 3, FUSED>(c, q, out, scale, st, in);
+    case 4: return launch_decode_t<D, 4, FUSED>(c, q, out, scale, st, in);
+    case 5: return launch_decode_t<D, 5, FUSED>(c, q, out, scale, st, in);
+    case 6: return launch_decode_t<D, 6, FUSED>(c, q, out, scale, st, in);
+    case 7: return launch_decode_t<D, 7, FUSED>(c, q, out, scale, st, in);
+    case 8: return launch_decode_t<D, 8, FUSED>(c, q, out, scale, st, in);
     default: return DMS_ERR_INVALID_ARG;
   }
 }
@@ -398,7 +431,8 @@ int dms_decode_attention(dms_cache_t* c, const void* q, float* out, float scale,
   if (!device_pointer_ok(q, c->device) || !device_pointer_ok(out, c->device)) return DMS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int G = q_heads / c->H;
-  return c->D == 128 ? launch_decode_d<128>(c, q, out, scale, G, st) : launch_decode_d<64>(c, q, out, scale, G, st);
+  return c->D == 128 ? launch_decode_d<128, false>(c, q, out, scale, G, st)
+                     : launch_decode_d<64, false>(c, q, out, scale, G, st);
 }
 
 int dms_step(dms_cache_t* c, const void* k, const void* v, const float* evict_logit, const void* q, float* out,
@@ -415,17 +449,16 @@ int dms_step(dms_cache_t* c, const void* k, const void* v, const float* evict_lo
       !device_pointer_ok(out, c->device))
     return DMS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int blocks = (c->NH * 32 + 255) / 256;
-  const uint4* k4 = static_cast<const uint4*>(k);
-  const uint4* v4 = static_cast<const uint4*>(v);
-  int rc = c->D == 128 ? launch_pdl(dms::append_kernel<128>, dim3(blocks), dim3(256), 0, st, c->view, k4, v4,
-                                    evict_logit, c->t)
-                       : launch_pdl(dms::append_kernel<64>, dim3(blocks), dim3(256), 0, st, c->view, k4, v4,
-                                    evict_logit, c->t);
+  // One launch: the decode kernel appends the token (into the halves of the
+  // double-buffered state that the step does not read) and attends over the
+  // cache after the append.
+  const StepInput in{static_cast<const uint4*>(k), static_cast<const uint4*>(v), evict_logit};
+  const int G = q_heads / c->H;
+  const int rc = c->D == 128 ? launch_decode_d<128, true>(c, q, out, scale, G, st, &in)
+                             : launch_decode_d<64, true>(c, q, out, scale, G, st, &in);
   if (rc != DMS_OK) return rc;
   c->t += 1;
-  const int G = q_heads / c->H;
-  return c->D == 128 ? launch_decode_d<128>(c, q, out, scale, G, st) : launch_decode_d<64>(c, q, out, scale, G, st);
+  return DMS_OK;
 }
 
 int dms_cache_lengths(dms_cache_t* c, int32_t* out_dev, void* stream) {

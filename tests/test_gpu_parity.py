@@ -354,27 +354,74 @@ def test_device_wait_time_limit_is_reported():
     tr.decode_and_compare(q, "after timeout")
 
 
-def test_step_equals_append_then_decode():
-    """dms_step (one call) gives the same outputs and cache state, bit for bit,
-    as dms_append followed by dms_decode_attention."""
-    wl = _small("step", 2, 8, 2, 128, 16, 300, ("normal", 0.6, 1.0), seed=13)
-    T = 260
-    a = Trajectory(wl, T)
+@pytest.mark.parametrize("case", [
+    # B, Hq, Hkv, D, w, cap, T, logits
+    (2, 8, 2, 128, 16, 300, 260, ("normal", 0.6, 1.0)),    # G 4: new slots inside tiles and at their edges
+    (3, 3, 3, 64, 1, 200, 150, ("normal", 0.0, 1.0)),      # MHA, d64, eager eviction
+    (2, 16, 2, 128, 40, 200, 180, ("normal", 1.15, 1.0)),  # G 8, window 40
+    (1, 10, 2, 64, 5, 100, 130, ("const", -10.0)),         # G 5, the cache fills at t = 100 (capacity error)
+    (128, 8, 8, 64, 1, 8, 40, ("const", 10.0)),            # 1024 heads of length 1: > 32 heads per warp
+])
+def test_step_equals_append_then_decode(case):
+    """dms_step (one launch: append + decode) gives the same outputs and cache
+    state, bit for bit, as dms_append followed by dms_decode_attention."""
+    B, Hq, Hkv, D, w, cap, T, logits = case
+    wl = _small("step", B, Hq, Hkv, D, w, cap, logits, seed=13)
+    k_all, v_all, lg_all = (x.cuda() for x in W.kv_range(wl, 0, 0, T))
+    q = W.q_range(wl, 0, 0, T).cuda()
+    a = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
     b = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
-    q = W.q_range(wl, 0, 0, T)
     out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
     for t in range(T):
-        k, v, lg = (a.k[:, :, t].contiguous().cuda(), a.v[:, :, t].contiguous().cuda(),
-                    a.lg[:, :, t].contiguous().cuda())
-        qt = q[:, :, t].contiguous().cuda()
-        a.cache.append(k, v, lg)
-        ref = a.cache.decode_attention(qt, scale=wl.scale)
+        k, v, lg = (k_all[:, :, t].contiguous(), v_all[:, :, t].contiguous(), lg_all[:, :, t].contiguous())
+        qt = q[:, :, t].contiguous()
+        a.append(k, v, lg)
+        ref = a.decode_attention(qt, scale=wl.scale)
         b.step(k, v, lg, qt, out, scale=wl.scale)
-        if t % 37 == 0 or t == T - 1:
-            assert torch.equal(out, ref), t
-    assert torch.equal(a.cache.lengths(), b.lengths())
-    assert torch.equal(a.cache.slot_positions(), b.slot_positions())
-    assert b.position == T and b.status() == dms.DMS_OK
+        assert torch.equal(out, ref), t
+    assert torch.equal(a.lengths(), b.lengths())
+    assert torch.equal(a.slot_positions(), b.slot_positions())
+    ka, va = a.export_kv()
+    kb, vb = b.export_kv()
+    assert torch.equal(ka, kb) and torch.equal(va, vb)
+    assert b.position == T and a.status() == b.status()
+    assert b.status() == (dms.DMS_ERR_CAPACITY if T > cap and logits[0] == "const" and logits[1] < 0 else dms.DMS_OK)
+    a.close()
+    b.close()
+
+
+def test_qwen3_8b_full_size_step_equals_append_then_decode():
+    """The benchmark's timed step at full size (B32, Hq32/Hkv8, d128, n=16384,
+    CR 8): 8 dms_step calls after a 16376-token history, against dms_append +
+    dms_decode_attention on a second cache with the same history; outputs and
+    bookkeeping bit-exact."""
+    wl = W.WORKLOADS["qwen3-8b"]
+    n_dec = 8
+    T0 = wl.cap - n_dec
+    a = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
+    b = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
+    for t0 in range(0, T0, wl.chunk):
+        t1 = min(T0, t0 + wl.chunk)
+        k, v, lg = W.kv_range(wl, 0, t0, t1, device="cuda")
+        a.append_chunk(k, v, lg)
+        b.append_chunk(k, v, lg)
+        del k, v, lg
+    k, v, lg = W.kv_range(wl, 0, T0, wl.cap, device="cuda")
+    q = W.q_range(wl, 0, T0, wl.cap, device="cuda")
+    out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    for j in range(n_dec):
+        kj, vj, lj, qj = (k[:, :, j].contiguous(), v[:, :, j].contiguous(), lg[:, :, j].contiguous(),
+                          q[:, :, j].contiguous())
+        a.append(kj, vj, lj)
+        ref = a.decode_attention(qj, scale=wl.scale)
+        b.step(kj, vj, lj, qj, out, scale=wl.scale)
+        assert torch.equal(out, ref), j
+    assert torch.equal(a.lengths(), b.lengths())
+    assert torch.equal(a.slot_positions(), b.slot_positions())
+    assert a.status() == b.status() == dms.DMS_OK
+    a.close()
+    b.close()
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("name,T", [("qwen3-8b-eager", 3000), ("qwen3-8b-w64", 3000), ("qwen3-8b-w256", 3000),
