@@ -189,8 +189,8 @@ class _Null:
 # the native arm
 # ---------------------------------------------------------------------------
 
-def fill_cache(dms, W, wl, n0, device, layer=0):
-    cache = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w, device=device)
+def fill_cache(dms, W, wl, n0, device, layer=0, kv_format="bf16"):
+    cache = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w, device=device, kv_format=kv_format)
     t = 0
     while t < n0:
         n = min(512, n0 - t)
@@ -456,6 +456,65 @@ def time_variants(dms, W, device, steps):
     return rows
 
 
+def decode_bytes_fp8(wl, len_sum):
+    """Algorithmic bytes of one decode call on an FP8 cache: per retained slot
+    the K row (D codes + its 16-byte scale chunk) and the V row (D codes); q,
+    out and lengths as for bf16."""
+    return len_sum * (2 * wl.D + 16) + wl.B * wl.Hq * wl.D * (2 + 4) + wl.B * wl.Hkv * 4
+
+
+def time_fp8_leg(dms, W, wl, device, steps):
+    """FP8 (E4M3) storage at the headline shapes: the cache is filled to
+    16384 - steps tokens, then `steps` timed dms_step calls (append + decode,
+    two launches for FP8 storage) and `steps` back-to-back dms_decode_attention
+    calls, with events around each pass."""
+    lib = dms.load_library()
+    stream = torch.cuda.current_stream(device)
+    n0 = wl.cap - steps - 3
+    cache = fill_cache(dms, W, wl, n0, device, kv_format="fp8")
+    qs, ks, vs, ls = step_inputs(W, wl, n0, steps + 3, device)
+    out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device=device)
+
+    def step(i):
+        rc = lib.dms_step(cache.handle, ks[i].data_ptr(), vs[i].data_ptr(), ls[i].data_ptr(), qs[i].data_ptr(),
+                          out.data_ptr(), wl.scale, wl.Hq, stream.cuda_stream)
+        if rc:
+            raise dms.DmsError(rc, "dms_step (fp8)")
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize(device)
+    len0 = int(cache.lengths().sum())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(3, steps + 3):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    step_us = e0.elapsed_time(e1) * 1e3 / steps
+    len1 = int(cache.lengths().sum())
+    e0.record(stream)
+    for _ in range(steps):
+        rc = lib.dms_decode_attention(cache.handle, qs[-1].data_ptr(), out.data_ptr(), wl.scale, wl.Hq,
+                                      stream.cuda_stream)
+        if rc:
+            raise dms.DmsError(rc, "dms_decode_attention (fp8)")
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    dec_us = e0.elapsed_time(e1) * 1e3 / steps
+    st = cache.status()
+    cache.close()
+    if st != dms.DMS_OK:
+        raise dms.DmsError(st, "fp8 leg")
+    alg = decode_bytes_fp8(wl, len1)
+    return {"storage": "fp8 e4m3, float32 scale per K row and V row", "ms_per_step": step_us * 1e-3,
+            "tokens_per_s": wl.B / (step_us * 1e-6),
+            "decode_us_per_launch_back_to_back": dec_us, "algorithmic_bytes_per_launch": alg,
+            "achieved_GBps": alg / (dec_us * 1e-6) / 1e9,
+            "kv_token_reads_per_step": 0.5 * (len0 + len1),
+            "note": "step = append kernel + decode kernel (the fused one-launch step is bf16 only)"}
+
+
 def measured_bf16_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -582,6 +641,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-storage leg")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill leg and print its figures (for profiling)")
     ap.add_argument("--prefill-chunks", type=int, default=9)
@@ -704,6 +764,10 @@ def main():
                                "(one copy), append + decode, output copied out, stream synchronized every step"}
     if not args.no_variants and world == 1:
         line["variants"] = time_variants(dms, W, device, 32)
+    if not args.no_fp8 and world == 1:
+        fp8 = time_fp8_leg(dms, W, wl, device, 64)
+        fp8["decode_speedup_over_bf16"] = r["decode_us"] / fp8["decode_us_per_launch_back_to_back"]
+        line["fp8"] = fp8
     if not args.no_prefill and world == 1:
         line["prefill"] = time_prefill_leg(dms, W, args.prefill_chunks, device)
     if not args.no_cpu_baseline and world == 1:

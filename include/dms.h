@@ -45,6 +45,10 @@ extern "C" {
 /* Largest query-head group per KV head (Hq / Hkv) the decode kernel supports. */
 #define DMS_MAX_GROUP 8
 
+/* Storage formats of the K and V pools (dms_cache_create_ex). */
+#define DMS_KV_BF16 0     /* bf16 rows, as given */
+#define DMS_KV_FP8_E4M3 1 /* FP8 E4M3 codes with a float32 scale per row */
+
 typedef struct dms_cache dms_cache_t;
 
 /*
@@ -60,6 +64,33 @@ typedef struct dms_cache dms_cache_t;
  * Returns NULL on failure; dms_last_error() then gives the code.
  */
 dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_dim, int window);
+
+/*
+ * As dms_cache_create, with the storage format of the K and V pools:
+ * DMS_KV_BF16 (what dms_cache_create makes) or DMS_KV_FP8_E4M3.
+ *
+ * FP8 storage combines the method's eviction with quantization, which the
+ * method's authors call orthogonal to it and combinable ("Inference-Time
+ * Hyper-Scaling with KV Cache Compression", paper-notes page, "Related work":
+ * KVQuant / KIVI).  Each retained K row and V row (one token, one KV head) is
+ * stored as head_dim E4M3 codes and a float32 scale:
+ *   scale = amax / 448 in float32 (amax = largest |x| of the row; 1 if amax = 0)
+ *   code  = E4M3(x / scale): float32 quotient, rounded to nearest (ties to
+ *           even) and saturated to +-448
+ * and stands for code * scale.  Inputs and outputs of every call stay bf16 /
+ * fp32 as documented; appends quantize, the decode attention dequantizes
+ * (scores and probabilities are computed in fp32 as for bf16 storage).  Pools:
+ * K rows of head_dim + 16 bytes (codes, then {K scale, V scale} and 8 bytes of
+ * padding), V rows of head_dim bytes, i.e. 2 * head_dim + 16 bytes per slot
+ * against 4 * head_dim for bf16.  On an FP8 cache dms_prefill returns
+ * DMS_ERR_INVALID_ARG (its tensor-core kernel reads bf16 rows), and dms_step
+ * runs as two launches (append, then decode).  dms_decode_attention_noalloc
+ * reads bf16 pools only.
+ */
+dms_cache_t* dms_cache_create_ex(int batch, int kv_heads, int capacity, int head_dim, int window, int kv_format);
+
+/* Storage format of a cache (DMS_KV_BF16 or DMS_KV_FP8_E4M3), or DMS_ERR_BAD_HANDLE. */
+int dms_cache_kv_format(dms_cache_t* cache);
 
 /* Code of the last failed dms_cache_create() on this thread (DMS_OK if none). */
 int dms_last_error(void);
@@ -122,8 +153,8 @@ int dms_prefill(dms_cache_t* cache, const void* q, const void* k, const void* v,
  * q_heads must be a multiple of kv_heads with q_heads / kv_heads <= 8.
  * The retained slots of all heads are split evenly across the warps of a
  * persistent grid (flash-decoding split-K balanced by retained length); the
- * partial results of a head split across warps are merged by a second kernel
- * enqueued right after it on the same stream.  Uses the split-K scratch that
+ * partial results of a head split across warps are merged in the same kernel
+ * by the last warp to finish that head.  Uses the split-K scratch that
  * dms_cache_create allocated; allocates nothing.  Returns DMS_ERR_EMPTY if
  * nothing was appended.
  */
@@ -148,8 +179,15 @@ int dms_cache_lengths(dms_cache_t* cache, int32_t* out_dev, void* stream);
 int dms_cache_slot_positions(dms_cache_t* cache, int32_t* out_dev, void* stream);
 
 /* Copy the K and V pools, in logical element order, into k_out / v_out
- * (bf16 [batch][kv_heads][capacity][head_dim] each, device memory). */
+ * (device memory, 16-byte aligned): bf16 [batch][kv_heads][capacity][head_dim]
+ * each; on an FP8 cache the E4M3 codes, uint8 [batch][kv_heads][capacity][head_dim]
+ * each (the scales: dms_cache_export_scales). */
 int dms_cache_export_kv(dms_cache_t* cache, void* k_out, void* v_out, void* stream);
+
+/* FP8 caches: copy the float32 scales of every slot's K row and V row into
+ * k_scale / v_scale (float32 [batch][kv_heads][capacity] each, device memory).
+ * DMS_ERR_INVALID_ARG on a bf16 cache. */
+int dms_cache_export_scales(dms_cache_t* cache, float* k_scale, float* v_scale, void* stream);
 
 /* Synchronize `stream`, then return the sticky device error (DMS_OK,
  * DMS_ERR_CAPACITY or DMS_ERR_TIMEOUT) or DMS_ERR_CUDA if the stream failed. */

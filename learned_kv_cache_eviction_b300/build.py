@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG_DIR, "libdms.so")
 SOURCES = ["dms_api.cu", "noalloc.cu"]
-HEADERS = ["append.cuh", "decode.cuh", "dms_device.cuh", "prefill.cuh", "umma.cuh"]
+HEADERS = ["append.cuh", "decode.cuh", "dms_device.cuh", "fp8.cuh", "prefill.cuh", "umma.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

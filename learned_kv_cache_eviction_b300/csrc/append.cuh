@@ -14,6 +14,7 @@
 #pragma once
 
 #include "dms_device.cuh"
+#include "fp8.cuh"
 
 namespace dms {
 
@@ -40,9 +41,10 @@ __device__ __forceinline__ int append_bookkeeping(const CacheView& c, int i, int
 }
 
 // One warp per (sequence, KV head).  Lane 0 does the bookkeeping; the warp
-// then copies the K row (chunk-permuted by slot) and the V row with 16-byte
-// stores.  k, v: [NH][D/8] chunks; logit: [NH].
-template <int D>
+// then stores the row: bf16, the K row (chunk-permuted by slot) and the V row
+// with 16-byte stores; fp8, both rows quantized.  k, v: [NH][D/8] chunks;
+// logit: [NH].
+template <int D, int KVF = kKvBf16>
 __global__ void __launch_bounds__(256) append_kernel(CacheView c, const uint4* __restrict__ k,
                                                      const uint4* __restrict__ v,
                                                      const float* __restrict__ logit, int64_t t) {
@@ -60,6 +62,15 @@ __global__ void __launch_bounds__(256) append_kernel(CacheView c, const uint4* _
   }
   s = __shfl_sync(0xffffffffu, s, 0);
   if (s < 0) return;
+  if constexpr (KVF == kKvFp8) {
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (lane < CH) x = __ldg(k + static_cast<size_t>(i) * CH + lane);
+    else if (lane < 2 * CH) x = __ldg(v + static_cast<size_t>(i) * CH + lane - CH);
+    const size_t slot = static_cast<size_t>(i) * c.cap + s;
+    quantize_kv_rows<D>(x, reinterpret_cast<uint8_t*>(c.K) + slot * (D + 16),
+                        reinterpret_cast<uint8_t*>(c.V) + slot * D, lane);
+    return;
+  }
   const size_t row = (static_cast<size_t>(i) * c.cap + s) * CH;
   if (lane < CH) {
     c.K[row + (lane ^ (s & 7))] = __ldg(k + static_cast<size_t>(i) * CH + lane);
@@ -164,8 +175,9 @@ __global__ void __launch_bounds__(128) append_chunk_slots_kernel(CacheView c, co
 // final position lies in [t0, t0 + chunk) receives that token's row (a token
 // retired within the same chunk is no longer in the map, so each slot is
 // written once).  Grid: (slot groups of 256, heads); one warp per 32 slots,
-// one coalesced row (K chunks permuted by slot, then V) per step.
-template <int D>
+// one coalesced row (K chunks permuted by slot, then V) per step; fp8 caches
+// quantize the row instead.
+template <int D, int KVF = kKvBf16>
 __global__ void __launch_bounds__(256) append_chunk_copy_kernel(CacheView c, const uint4* __restrict__ k,
                                                                 const uint4* __restrict__ v, int64_t t0,
                                                                 int chunk) {
@@ -186,6 +198,15 @@ __global__ void __launch_bounds__(256) append_chunk_copy_kernel(CacheView c, con
     const int ss = s0 + src;
     const int tok = __shfl_sync(0xffffffffu, p, src) - static_cast<int>(t0);
     const size_t in = (static_cast<size_t>(i) * chunk + tok) * CH;
+    if constexpr (KVF == kKvFp8) {
+      uint4 x = make_uint4(0u, 0u, 0u, 0u);
+      if (lane < CH) x = __ldg(k + in + lane);
+      else if (lane < 2 * CH) x = __ldg(v + in + lane - CH);
+      const size_t slot = static_cast<size_t>(i) * c.cap + ss;
+      quantize_kv_rows<D>(x, reinterpret_cast<uint8_t*>(c.K) + slot * (D + 16),
+                          reinterpret_cast<uint8_t*>(c.V) + slot * D, lane);
+      continue;
+    }
     const size_t row = (static_cast<size_t>(i) * c.cap + ss) * CH;
     if (lane < CH) {
       c.K[row + (lane ^ (ss & 7))] = __ldg(k + in + lane);
@@ -212,9 +233,21 @@ __global__ void wait_selftest_kernel(int32_t* err) {
 }
 
 // Logical-order copy of the K and V pools (undoes the chunk permutation of K).
-// One thread per 16-byte chunk.
-template <int D>
+// One thread per 16-byte chunk.  fp8: the codes only, [NH][cap][D] bytes each
+// (export_scales_kernel copies the scales).
+template <int D, int KVF = kKvBf16>
 __global__ void export_kv_kernel(CacheView c, uint4* __restrict__ k_out, uint4* __restrict__ v_out) {
+  if constexpr (KVF == kKvFp8) {
+    constexpr int U = D / 16;  // 16-byte chunks of codes per row
+    const size_t n = static_cast<size_t>(c.NH) * c.cap * U;
+    for (size_t x = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; x < n;
+         x += static_cast<size_t>(gridDim.x) * blockDim.x) {
+      const size_t row = x / U;
+      k_out[x] = c.K[row * (U + 1) + x % U];
+      v_out[x] = c.V[x];
+    }
+    return;
+  }
   constexpr int CH = D / 8;
   const size_t n = static_cast<size_t>(c.NH) * c.cap * CH;
   for (size_t x = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; x < n;
@@ -224,6 +257,18 @@ __global__ void export_kv_kernel(CacheView c, uint4* __restrict__ k_out, uint4* 
     const int s = static_cast<int>(row % c.cap);
     k_out[x] = c.K[row * CH + (ch ^ (s & 7))];
     v_out[x] = c.V[x];
+  }
+}
+
+// fp8 caches: the K and V scales of every slot, [NH][cap] float32 each.
+template <int D>
+__global__ void export_scales_kernel(CacheView c, float* __restrict__ k_scale, float* __restrict__ v_scale) {
+  const size_t n = static_cast<size_t>(c.NH) * c.cap;
+  for (size_t x = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; x < n;
+       x += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float2 sc = *reinterpret_cast<const float2*>(reinterpret_cast<const uint8_t*>(c.K) + x * (D + 16) + D);
+    k_scale[x] = sc.x;
+    v_scale[x] = sc.y;
   }
 }
 

@@ -32,20 +32,29 @@
 #pragma once
 
 #include "dms_device.cuh"
+#include "fp8.cuh"
 
 namespace dms {
 
-template <int D_, int G_>
+template <int D_, int G_, int KVF_ = kKvBf16>
 struct DecodeShape {
   static constexpr int D = D_;
   static constexpr int G = G_;
-  static constexpr int TK = 16;      // slots per tile
-  static constexpr int NST = 2;      // tiles in flight per warp
-  static constexpr int CH = D / 8;   // 16-byte chunks per K/V row
-  static constexpr int HCH = CH / 2; // chunks per half row (two lanes score one slot)
-  static constexpr int EL = D / 32;  // output elements per lane in PV
-  static constexpr int ROWB = D * 2;
-  static constexpr int TILEB = TK * ROWB;
+  static constexpr int KVF = KVF_;
+  static constexpr bool FP8 = KVF == kKvFp8;
+  static constexpr int TK = 16;                 // slots per tile
+  static constexpr int NST = FP8 ? 3 : 2;       // tiles in flight per warp
+  static constexpr int CH = D / 8;              // 16-byte chunks per bf16 row
+  static constexpr int HCH = CH / 2;            // chunks per half row (two lanes score one slot)
+  static constexpr int EL = D / 32;             // output elements per lane in PV
+  // Row bytes in HBM and in the tiles: bf16 2 D each; fp8 D codes, the K row
+  // followed by its 16-byte scale chunk.
+  static constexpr int ROWB_K = FP8 ? D + 16 : 2 * D;
+  static constexpr int ROWB_V = FP8 ? D : 2 * D;
+  static constexpr int KU4 = ROWB_K / 16;       // 16-byte units per row
+  static constexpr int VU4 = ROWB_V / 16;
+  static constexpr int TILEB_K = TK * ROWB_K;
+  static constexpr int TILEB_V = TK * ROWB_V;
   // qs: fp32 q, per head g two half rows of D/2 floats, padded by 4 floats so
   // that the two lane halves read different banks.
   static constexpr int QHALF = D / 2 + 4;
@@ -54,8 +63,8 @@ struct DecodeShape {
   // packed fp32 FMA), padded to a multiple of 4 floats.
   static constexpr int PROW = (2 * G + 3) / 4 * 4;
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = NST * TILEB;
-  static constexpr int OFF_QS = 2 * NST * TILEB;
+  static constexpr int OFF_V = NST * TILEB_K;
+  static constexpr int OFF_QS = NST * (TILEB_K + TILEB_V);
   static constexpr int QV = (G * D / 8 + 31) / 32;  // 16-byte q chunks per lane
   static constexpr int OFF_P = OFF_QS + ((G * QROW * 4 + 15) / 16) * 16;
   static constexpr int OFF_BAR = OFF_P + TK * PROW * 4;
@@ -65,7 +74,8 @@ struct DecodeShape {
   static constexpr int FX_HEADS = 14;
   static constexpr int FX_I0 = FX_HEADS, FX_SEG = FX_HEADS + 1;
   static constexpr int OFF_FX = OFF_BAR + NST * 8;
-  static constexpr int WARP_BYTES = ((OFF_FX + (FX_HEADS + 2) * 4 + 127) / 128) * 128;
+  static constexpr int FX_BYTES = FP8 ? 0 : (FX_HEADS + 2) * 4;  // the fused step is bf16 only
+  static constexpr int WARP_BYTES = ((OFF_FX + FX_BYTES + 127) / 128) * 128;
   static constexpr int kSmemBudget = 227 * 1024 - 1024;  // leaves room for static shared memory
   // Warps per CTA: 12 (three per scheduler) where the shared memory allows.  With
   // three warps on a scheduler its register file leaves 168 registers per thread;
@@ -329,11 +339,13 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, size_t base,
   }
 }
 
-template <int D, int G, bool FUSED>
-__global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(const DecodeArgs a) {
-  using Sh = DecodeShape<D, G>;
+template <int D, int G, bool FUSED, int KVF = kKvBf16>
+__global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_kernel(const DecodeArgs a) {
+  using Sh = DecodeShape<D, G, KVF>;
+  static_assert(!(FUSED && Sh::FP8), "the fused step stores bf16 rows");
   constexpr int NW = Sh::NW, TK = Sh::TK, NST = Sh::NST, CH = Sh::CH, HCH = Sh::HCH, EL = Sh::EL;
-  constexpr int ROWB = Sh::ROWB, TILEB = Sh::TILEB, QHALF = Sh::QHALF, QROW = Sh::QROW, PROW = Sh::PROW;
+  constexpr int ROWB_K = Sh::ROWB_K, ROWB_V = Sh::ROWB_V, TILEB_K = Sh::TILEB_K, TILEB_V = Sh::TILEB_V;
+  constexpr int QHALF = Sh::QHALF, QROW = Sh::QROW, PROW = Sh::PROW;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   // Launched as a programmatic dependent of the previous kernel: everything the
@@ -472,11 +484,11 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
       const int cnt = min(TK, is.send - is.s);
       const int buf = n_issued % NST;
       if (lane == 0) {
-        const uint32_t bytes = static_cast<uint32_t>(cnt * ROWB);
+        const uint32_t kbytes = static_cast<uint32_t>(cnt * ROWB_K), vbytes = static_cast<uint32_t>(cnt * ROWB_V);
         const size_t row = static_cast<size_t>(is.i) * a.cap + is.s;
-        mbar_arrive_expect_tx(&bars[buf], 2 * bytes);
-        bulk_copy_g2s(Ks + buf * TILEB, a.K + row * CH, bytes, &bars[buf]);
-        bulk_copy_g2s(Vs + buf * TILEB, a.V + row * CH, bytes, &bars[buf]);
+        mbar_arrive_expect_tx(&bars[buf], kbytes + vbytes);
+        bulk_copy_g2s(Ks + buf * TILEB_K, a.K + row * Sh::KU4, kbytes, &bars[buf]);
+        bulk_copy_g2s(Vs + buf * TILEB_V, a.V + row * Sh::VU4, vbytes, &bars[buf]);
       }
       if (is.first) {
         const int b = is.i / a.Hkv, h = is.i - (is.i / a.Hkv) * a.Hkv;
@@ -558,14 +570,15 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
     if constexpr (FUSED) {
       const int sw = fx[Sh::FX_SEG];  // reloaded after the wait (the wait clobbers memory)
       if (static_cast<unsigned>(sw - s0) < static_cast<unsigned>(cnt))
-        patch_new_row(a, reinterpret_cast<uint4*>(Ks + buf * TILEB), reinterpret_cast<uint4*>(Vs + buf * TILEB),
+        patch_new_row(a, reinterpret_cast<uint4*>(Ks + buf * TILEB_K), reinterpret_cast<uint4*>(Vs + buf * TILEB_V),
                       seg_i, sw - s0, sw, CH, lane);
     }
 
     // ---- QK: lanes r and r + 16 score slot s0 + r over the two halves of D ----
     float sc[G];
-    {
-      const uint4* krow = reinterpret_cast<const uint4*>(Ks + buf * TILEB) + r * CH;
+    float vsc = 0.f;  // fp8: the slot's V scale (folded into its probability)
+    if constexpr (!Sh::FP8) {
+      const uint4* krow = reinterpret_cast<const uint4*>(Ks + buf * TILEB_K) + r * CH;
       const int sw = (s0 + r) & 7;
       const float* qh = qs + hf * QHALF;
       float2 acc0[G], acc1[G];
@@ -597,6 +610,48 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
         sg += __shfl_xor_sync(0xffffffffu, sg, 16);
         sc[g] = r < cnt ? sg : -INFINITY;
       }
+    } else {
+      // fp8: the lane's half row is D / 32 units of 16 codes; the score is the
+      // dot product with the codes times the row's K scale.
+      const uint8_t* krow = Ks + buf * TILEB_K + r * ROWB_K;
+      const float* qh = qs + hf * QHALF;
+      float2 acc0[G], acc1[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        acc0[g] = make_float2(0.f, 0.f);
+        acc1[g] = make_float2(0.f, 0.f);
+      }
+      float ksc = 0.f;
+      if (r < cnt) {
+        const float2 kv = *reinterpret_cast<const float2*>(krow + D);
+        ksc = kv.x;
+        vsc = kv.y;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          const uint4 kk = *reinterpret_cast<const uint4*>(krow + hf * (D / 2) + c * 16);
+#pragma unroll
+          for (int hw = 0; hw < 2; ++hw) {  // 8 codes at a time
+            const uint32_t w0 = hw ? kk.z : kk.x, w1 = hw ? kk.w : kk.y;
+            const float2 k0 = e4m3x2_to_float2(w0 & 0xffffu), k1 = e4m3x2_to_float2(w0 >> 16);
+            const float2 k2 = e4m3x2_to_float2(w1 & 0xffffu), k3 = e4m3x2_to_float2(w1 >> 16);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const float4* qp = reinterpret_cast<const float4*>(qh + g * QROW + c * 16 + hw * 8);
+              const float4 qa = qp[0], qb = qp[1];
+              acc0[g] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc0[g]);
+              acc1[g] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc1[g]);
+              acc0[g] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc0[g]);
+              acc1[g] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc1[g]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float sg = (acc0[g].x + acc0[g].y) + (acc1[g].x + acc1[g].y);
+        sg += __shfl_xor_sync(0xffffffffu, sg, 16);
+        sc[g] = r < cnt ? sg * ksc : -INFINITY;
+      }
     }
 
     // ---- online softmax (base 2); lanes r and r + 16 hold the same scores ----
@@ -616,9 +671,13 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
         rescale |= alpha[g] != 1.f;
       }
       if (hf == 0) {
+        // fp8: the weight of the slot's V codes is its probability times its V scale
         float2* prow = reinterpret_cast<float2*>(pb + r * PROW);
 #pragma unroll
-        for (int g = 0; g < G; ++g) prow[g] = make_float2(p[g], p[g]);
+        for (int g = 0; g < G; ++g) {
+          const float pw = Sh::FP8 ? p[g] * vsc : p[g];
+          prow[g] = make_float2(pw, pw);
+        }
       }
       if (rescale) {
 #pragma unroll
@@ -633,15 +692,23 @@ __global__ void __launch_bounds__(DecodeShape<D, G>::NW * 32, 1) decode_kernel(c
 
     // ---- PV: lane owns elements [lane*EL, lane*EL + EL) of every head ----
     {
-      const uint8_t* Vt = Vs + buf * TILEB + lane * (EL * 2);
+      const uint8_t* Vt = Vs + buf * TILEB_V + lane * (EL * (Sh::FP8 ? 1 : 2));
       auto pv_row = [&](int j) {
         float2 v2[EL / 2];
-        if constexpr (EL == 4) {
-          const uint2 vv = *reinterpret_cast<const uint2*>(Vt + j * ROWB);
+        if constexpr (Sh::FP8) {
+          if constexpr (EL == 4) {
+            const uint32_t vv = *reinterpret_cast<const uint32_t*>(Vt + j * ROWB_V);
+            v2[0] = e4m3x2_to_float2(vv & 0xffffu);
+            v2[1] = e4m3x2_to_float2(vv >> 16);
+          } else {
+            v2[0] = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(Vt + j * ROWB_V));
+          }
+        } else if constexpr (EL == 4) {
+          const uint2 vv = *reinterpret_cast<const uint2*>(Vt + j * ROWB_V);
           v2[0] = bf16x2_to_float2(vv.x);
           v2[1] = bf16x2_to_float2(vv.y);
         } else {
-          v2[0] = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(Vt + j * ROWB));
+          v2[0] = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(Vt + j * ROWB_V));
         }
         const float4* prow = reinterpret_cast<const float4*>(pb + j * PROW);
 #pragma unroll

@@ -19,6 +19,7 @@
 
 struct dms_cache {
   int B, H, cap, D, w, NH;
+  int kvf;  // DMS_KV_BF16 or DMS_KV_FP8_E4M3
   int64_t t;
   int device;
   int num_sms;
@@ -108,12 +109,12 @@ struct StepInput {
 // stands at position c->t.  Fused (FUSED true, `in` set): the token of
 // position c->t is appended in the same launch and the attention runs over
 // the cache after it; the caller then advances c->t.
-template <int D, int G, bool FUSED>
+template <int D, int G, bool FUSED, int KVF>
 int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaStream_t st, const StepInput* in) {
-  using Sh = dms::DecodeShape<D, G>;
+  using Sh = dms::DecodeShape<D, G, KVF>;
   static bool attr_done[64] = {};
   if (c->device < 64 && !attr_done[c->device]) {
-    if (cudaFuncSetAttribute(dms::decode_kernel<D, G, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(dms::decode_kernel<D, G, FUSED, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Sh::SMEM) != cudaSuccess)
       return DMS_ERR_CUDA;
     attr_done[c->device] = true;
@@ -159,21 +160,21 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
     a.slot_pos = c->view.slot_pos;
     a.len_new = dms::len_after(c->view, c->t + 1);
   }
-  return launch_pdl(dms::decode_kernel<D, G, FUSED>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
+  return launch_pdl(dms::decode_kernel<D, G, FUSED, KVF>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
 }
 
-template <int D, bool FUSED>
+template <int D, bool FUSED, int KVF = dms::kKvBf16>
 int launch_decode_d(dms_cache* c, const void* q, float* out, float scale, int G, cudaStream_t st,
                     const StepInput* in = nullptr) {
   switch (G) {
-    case 1: return launch_decode_t<D, 1, FUSED>(c, q, out, scale, st, in);
-    case 2: return launch_decode_t<D, 2, FUSED>(c, q, out, scale, st, in);
-    case 3: return launch_decode_t<D, 3, FUSED>(c, q, out, scale, st, in);
-    case 4: return launch_decode_t<D, 4, FUSED>(c, q, out, scale, st, in);
-    case 5: return launch_decode_t<D, 5, FUSED>(c, q, out, scale, st, in);
-    case 6: return launch_decode_t<D, 6, FUSED>(c, q, out, scale, st, in);
-    case 7: return launch_decode_t<D, 7, FUSED>(c, q, out, scale, st, in);
-    case 8: return launch_decode_t<D, 8, FUSED>(c, q, out, scale, st, in);
+    case 1: return launch_decode_t<D, 1, FUSED, KVF>(c, q, out, scale, st, in);
+    case 2: return launch_decode_t<D, 2, FUSED, KVF>(c, q, out, scale, st, in);
+    case 3: return launch_decode_t<D, 3, FUSED, KVF>(c, q, out, scale, st, in);
+    case 4: return launch_decode_t<D, 4, FUSED, KVF>(c, q, out, scale, st, in);
+    case 5: return launch_decode_t<D, 5, FUSED, KVF>(c, q, out, scale, st, in);
+    case 6: return launch_decode_t<D, 6, FUSED, KVF>(c, q, out, scale, st, in);
+    case 7: return launch_decode_t<D, 7, FUSED, KVF>(c, q, out, scale, st, in);
+    case 8: return launch_decode_t<D, 8, FUSED, KVF>(c, q, out, scale, st, in);
     default: return DMS_ERR_INVALID_ARG;
   }
 }
@@ -215,6 +216,31 @@ int launch_prefill_d(dms_cache* c, const dms::PrefillArgs& a, int G, cudaStream_
   }
 }
 
+// Decode launch for the cache's storage format.
+template <int D, bool FUSED>
+int launch_decode_f(dms_cache* c, const void* q, float* out, float scale, int G, cudaStream_t st,
+                    const StepInput* in = nullptr) {
+  return c->kvf == DMS_KV_FP8_E4M3 ? launch_decode_d<D, false, dms::kKvFp8>(c, q, out, scale, G, st)
+                                   : launch_decode_d<D, FUSED, dms::kKvBf16>(c, q, out, scale, G, st, in);
+}
+
+// Single-token append (one warp per head) for the cache's head dim and format.
+int launch_append(dms_cache* c, const void* k, const void* v, const float* logit, cudaStream_t st) {
+  const int blocks = (c->NH * 32 + 255) / 256;
+  const uint4* k4 = static_cast<const uint4*>(k);
+  const uint4* v4 = static_cast<const uint4*>(v);
+  const bool fp8 = c->kvf == DMS_KV_FP8_E4M3;
+  if (c->D == 128)
+    return fp8 ? launch_pdl(dms::append_kernel<128, dms::kKvFp8>, dim3(blocks), dim3(256), 0, st, c->view, k4, v4,
+                            logit, c->t)
+               : launch_pdl(dms::append_kernel<128, dms::kKvBf16>, dim3(blocks), dim3(256), 0, st, c->view, k4, v4,
+                            logit, c->t);
+  return fp8 ? launch_pdl(dms::append_kernel<64, dms::kKvFp8>, dim3(blocks), dim3(256), 0, st, c->view, k4, v4, logit,
+                          c->t)
+             : launch_pdl(dms::append_kernel<64, dms::kKvBf16>, dim3(blocks), dim3(256), 0, st, c->view, k4, v4,
+                          logit, c->t);
+}
+
 // Chunk append: the bookkeeping (one warp per head), then the row copy.
 int launch_append_chunk(dms_cache* c, const void* k, const void* v, const float* logits, int chunk, cudaStream_t st) {
   const int rc = launch_pdl(dms::append_chunk_slots_kernel, dim3((c->NH + 3) / 4), dim3(128), 0, st, c->view, logits,
@@ -223,10 +249,16 @@ int launch_append_chunk(dms_cache* c, const void* k, const void* v, const float*
   const dim3 grid((c->cap + 255) / 256, c->NH);
   const uint4* k4 = static_cast<const uint4*>(k);
   const uint4* v4 = static_cast<const uint4*>(v);
-  return c->D == 128 ? launch_pdl(dms::append_chunk_copy_kernel<128>, grid, dim3(256), 0, st, c->view, k4, v4, c->t,
-                                  chunk)
-                     : launch_pdl(dms::append_chunk_copy_kernel<64>, grid, dim3(256), 0, st, c->view, k4, v4, c->t,
-                                  chunk);
+  const bool fp8 = c->kvf == DMS_KV_FP8_E4M3;
+  if (c->D == 128)
+    return fp8 ? launch_pdl(dms::append_chunk_copy_kernel<128, dms::kKvFp8>, grid, dim3(256), 0, st, c->view, k4, v4,
+                            c->t, chunk)
+               : launch_pdl(dms::append_chunk_copy_kernel<128, dms::kKvBf16>, grid, dim3(256), 0, st, c->view, k4, v4,
+                            c->t, chunk);
+  return fp8 ? launch_pdl(dms::append_chunk_copy_kernel<64, dms::kKvFp8>, grid, dim3(256), 0, st, c->view, k4, v4,
+                          c->t, chunk)
+             : launch_pdl(dms::append_chunk_copy_kernel<64, dms::kKvBf16>, grid, dim3(256), 0, st, c->view, k4, v4,
+                          c->t, chunk);
 }
 
 void free_cache_memory(dms_cache* c) {
@@ -263,8 +295,13 @@ const char* dms_error_string(int code) {
 }
 
 dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_dim, int window) {
+  return dms_cache_create_ex(batch, kv_heads, capacity, head_dim, window, DMS_KV_BF16);
+}
+
+dms_cache_t* dms_cache_create_ex(int batch, int kv_heads, int capacity, int head_dim, int window, int kv_format) {
   g_last_error = DMS_OK;
-  if (batch < 1 || kv_heads < 1 || capacity < 1 || window < 1 || (head_dim != 64 && head_dim != 128)) {
+  if (batch < 1 || kv_heads < 1 || capacity < 1 || window < 1 || (head_dim != 64 && head_dim != 128) ||
+      (kv_format != DMS_KV_BF16 && kv_format != DMS_KV_FP8_E4M3)) {
     g_last_error = DMS_ERR_INVALID_ARG;
     return nullptr;
   }
@@ -286,6 +323,7 @@ dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_di
   c->D = head_dim;
   c->w = window;
   c->NH = static_cast<int>(NH);
+  c->kvf = kv_format;
   c->t = 0;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
@@ -294,20 +332,23 @@ dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_di
     g_last_error = DMS_ERR_CUDA;
     return nullptr;
   }
-  const size_t pool = static_cast<size_t>(NH) * capacity * head_dim * 2;
+  // bytes per slot: bf16 2 D per row; fp8 D codes per row, plus the K row's 16-byte scale chunk
+  const bool fp8 = kv_format == DMS_KV_FP8_E4M3;
+  const size_t kpool = static_cast<size_t>(NH) * capacity * (fp8 ? head_dim + 16 : 2 * head_dim);
+  const size_t vpool = static_cast<size_t>(NH) * capacity * (fp8 ? head_dim : 2 * head_dim);
   const size_t nslot = static_cast<size_t>(NH) * capacity;
   const size_t nring = 2 * static_cast<size_t>(NH) * window;  // two generations
   c->part_entries = static_cast<size_t>(c->num_sms) * dms::kMaxWarpsPerCta + NH;
   const size_t part_acc = c->part_entries * DMS_MAX_GROUP * head_dim * sizeof(float);
   const size_t part_ml = c->part_entries * DMS_MAX_GROUP * 2 * sizeof(float);
-  bool ok = cudaMalloc(&c->view.K, pool) == cudaSuccess && cudaMalloc(&c->view.V, pool) == cudaSuccess &&
+  bool ok = cudaMalloc(&c->view.K, kpool) == cudaSuccess && cudaMalloc(&c->view.V, vpool) == cudaSuccess &&
             cudaMalloc(&c->view.slot_pos, nslot * 4) == cudaSuccess &&
             cudaMalloc(&c->view.ring_slot, nring * 4) == cudaSuccess &&
             cudaMalloc(&c->view.ring_flag, nring) == cudaSuccess &&
             cudaMalloc(&c->view.len, 2 * NH * 4) == cudaSuccess && cudaMalloc(&c->view.err, kAlign) == cudaSuccess &&
             cudaMalloc(&c->part_acc, part_acc) == cudaSuccess && cudaMalloc(&c->part_ml, part_ml) == cudaSuccess &&
             cudaMalloc(&c->head_cnt, NH * 4) == cudaSuccess;
-  ok = ok && cudaMemset(c->view.K, 0, pool) == cudaSuccess && cudaMemset(c->view.V, 0, pool) == cudaSuccess &&
+  ok = ok && cudaMemset(c->view.K, 0, kpool) == cudaSuccess && cudaMemset(c->view.V, 0, vpool) == cudaSuccess &&
        cudaMemset(c->view.slot_pos, 0xff, nslot * 4) == cudaSuccess &&
        cudaMemset(c->view.ring_slot, 0xff, nring * 4) == cudaSuccess &&
        cudaMemset(c->view.ring_flag, 0, nring) == cudaSuccess && cudaMemset(c->view.len, 0, 2 * NH * 4) == cudaSuccess &&
@@ -324,6 +365,7 @@ dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_di
   c->view.cap = capacity;
   c->view.D = head_dim;
   c->view.w = window;
+  c->view.kvf = fp8 ? dms::kKvFp8 : dms::kKvBf16;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     g_live.insert(c);
@@ -353,16 +395,7 @@ int dms_append(dms_cache_t* c, const void* k, const void* v, const float* evict_
   if (!device_pointer_ok(k, c->device) || !device_pointer_ok(v, c->device) ||
       !device_pointer_ok(evict_logit, c->device))
     return DMS_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int threads = 256;
-  const int blocks = (c->NH * 32 + threads - 1) / threads;
-  const uint4* k4 = static_cast<const uint4*>(k);
-  const uint4* v4 = static_cast<const uint4*>(v);
-  const int rc = c->D == 128
-                     ? launch_pdl(dms::append_kernel<128>, dim3(blocks), dim3(threads), 0, st, c->view, k4, v4,
-                                  evict_logit, c->t)
-                     : launch_pdl(dms::append_kernel<64>, dim3(blocks), dim3(threads), 0, st, c->view, k4, v4,
-                                  evict_logit, c->t);
+  const int rc = launch_append(c, k, v, evict_logit, static_cast<cudaStream_t>(stream));
   if (rc == DMS_OK) c->t += 1;
   return rc;
 }
@@ -385,7 +418,8 @@ int dms_prefill(dms_cache_t* c, const void* q, const void* k, const void* v, con
   if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
   if (chunk < 1 || !q || !k || !v || !logits || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
       !aligned16(logits) || !aligned16(out) || q_heads < 1 || q_heads % c->H != 0 ||
-      q_heads / c->H > DMS_MAX_GROUP || !std::isfinite(scale) || c->t + chunk > INT32_MAX)
+      q_heads / c->H > DMS_MAX_GROUP || !std::isfinite(scale) || c->t + chunk > INT32_MAX ||
+      c->kvf != DMS_KV_BF16)
     return DMS_ERR_INVALID_ARG;
   DeviceGuard g(c->device);
   if (!g.ok) return DMS_ERR_CUDA;
@@ -431,8 +465,8 @@ int dms_decode_attention(dms_cache_t* c, const void* q, float* out, float scale,
   if (!device_pointer_ok(q, c->device) || !device_pointer_ok(out, c->device)) return DMS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int G = q_heads / c->H;
-  return c->D == 128 ? launch_decode_d<128, false>(c, q, out, scale, G, st)
-                     : launch_decode_d<64, false>(c, q, out, scale, G, st);
+  return c->D == 128 ? launch_decode_f<128, false>(c, q, out, scale, G, st)
+                     : launch_decode_f<64, false>(c, q, out, scale, G, st);
 }
 
 int dms_step(dms_cache_t* c, const void* k, const void* v, const float* evict_logit, const void* q, float* out,
@@ -449,13 +483,21 @@ int dms_step(dms_cache_t* c, const void* k, const void* v, const float* evict_lo
       !device_pointer_ok(out, c->device))
     return DMS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // One launch: the decode kernel appends the token (into the halves of the
-  // double-buffered state that the step does not read) and attends over the
-  // cache after the append.
-  const StepInput in{static_cast<const uint4*>(k), static_cast<const uint4*>(v), evict_logit};
   const int G = q_heads / c->H;
-  const int rc = c->D == 128 ? launch_decode_d<128, true>(c, q, out, scale, G, st, &in)
-                             : launch_decode_d<64, true>(c, q, out, scale, G, st, &in);
+  if (c->kvf == DMS_KV_FP8_E4M3) {
+    // fp8 caches: the append kernel, then the decode kernel
+    int rc = launch_append(c, k, v, evict_logit, st);
+    if (rc != DMS_OK) return rc;
+    c->t += 1;
+    return c->D == 128 ? launch_decode_f<128, false>(c, q, out, scale, G, st)
+                       : launch_decode_f<64, false>(c, q, out, scale, G, st);
+  }
+  // bf16: one launch.  The decode kernel appends the token (into the halves of
+  // the double-buffered state that the step does not read) and attends over
+  // the cache after the append.
+  const StepInput in{static_cast<const uint4*>(k), static_cast<const uint4*>(v), evict_logit};
+  const int rc = c->D == 128 ? launch_decode_f<128, true>(c, q, out, scale, G, st, &in)
+                             : launch_decode_f<64, true>(c, q, out, scale, G, st, &in);
   if (rc != DMS_OK) return rc;
   c->t += 1;
   return DMS_OK;
@@ -490,12 +532,34 @@ int dms_cache_export_kv(dms_cache_t* c, void* k_out, void* v_out, void* stream) 
   if (!device_pointer_ok(k_out, c->device) || !device_pointer_ok(v_out, c->device)) return DMS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int blocks = c->num_sms * 8;
-  if (c->D == 128)
-    dms::export_kv_kernel<128><<<blocks, 256, 0, st>>>(c->view, static_cast<uint4*>(k_out), static_cast<uint4*>(v_out));
-  else
-    dms::export_kv_kernel<64><<<blocks, 256, 0, st>>>(c->view, static_cast<uint4*>(k_out), static_cast<uint4*>(v_out));
+  uint4* ko = static_cast<uint4*>(k_out);
+  uint4* vo = static_cast<uint4*>(v_out);
+  const bool fp8 = c->kvf == DMS_KV_FP8_E4M3;
+  if (c->D == 128) {
+    if (fp8) dms::export_kv_kernel<128, dms::kKvFp8><<<blocks, 256, 0, st>>>(c->view, ko, vo);
+    else dms::export_kv_kernel<128, dms::kKvBf16><<<blocks, 256, 0, st>>>(c->view, ko, vo);
+  } else {
+    if (fp8) dms::export_kv_kernel<64, dms::kKvFp8><<<blocks, 256, 0, st>>>(c->view, ko, vo);
+    else dms::export_kv_kernel<64, dms::kKvBf16><<<blocks, 256, 0, st>>>(c->view, ko, vo);
+  }
   return launch_status();
 }
+
+int dms_cache_export_scales(dms_cache_t* c, float* k_scale, float* v_scale, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  if (!k_scale || !v_scale || c->kvf != DMS_KV_FP8_E4M3) return DMS_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!device_pointer_ok(k_scale, c->device) || !device_pointer_ok(v_scale, c->device)) return DMS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int blocks = c->num_sms * 8;
+  if (c->D == 128)
+    dms::export_scales_kernel<128><<<blocks, 256, 0, st>>>(c->view, k_scale, v_scale);
+  else
+    dms::export_scales_kernel<64><<<blocks, 256, 0, st>>>(c->view, k_scale, v_scale);
+  return launch_status();
+}
+
+int dms_cache_kv_format(dms_cache_t* c) { return is_live(c) ? c->kvf : DMS_ERR_BAD_HANDLE; }
 
 int dms_cache_selftest_wait(dms_cache_t* c, void* stream) {
   if (!is_live(c)) return DMS_ERR_BAD_HANDLE;

@@ -24,15 +24,25 @@ constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;
 // step's old state from every CTA while it writes the new state (the fused
 // append + decode step): the lengths after t appends are len[t & 1], and the
 // ring entry (slot, mark) of position p is ring[(p / w) & 1][i][p % w].
+//
+// FP8 storage (kvf == kKvFp8): a K row is D E4M3 codes followed by one 16-byte
+// chunk {K scale, V scale, 0, 0} (float32); a V row is D codes.  The K row
+// stride, D + 16 bytes, is an odd number of 16-byte chunks, so 8 consecutive
+// rows read at the same column fall into 8 different bank groups with no
+// permutation.
+constexpr int kKvBf16 = 0;
+constexpr int kKvFp8 = 1;
+
 struct CacheView {
-  uint4* K;            // [NH][cap][D/8] 16-byte chunks (bf16 x 8)
-  uint4* V;            // [NH][cap][D/8]
+  uint4* K;            // bf16: [NH][cap][D/8] 16-byte chunks (bf16 x 8); fp8: [NH][cap][D/16 + 1]
+  uint4* V;            // bf16: [NH][cap][D/8]; fp8: [NH][cap][D/16]
   int32_t* slot_pos;   // [NH][cap]
   int32_t* ring_slot;  // [2][NH][w]
   uint8_t* ring_flag;  // [2][NH][w]
   int32_t* len;        // [2][NH]
   int32_t* err;        // sticky error bits
   int NH, cap, D, w;
+  int kvf;  // kKvBf16 or kKvFp8
 };
 
 // Lengths after t appends.

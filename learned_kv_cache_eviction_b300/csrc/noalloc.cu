@@ -105,7 +105,7 @@ int run(int dev, int num_sms, unsigned char* scratch, const void* k_pool, const 
   const size_t ml_bytes = entries * G * 2 * sizeof(float);
   if (acc_off + acc_bytes + ml_bytes > kScratchBytes) return DMS_ERR_SCRATCH_LIMIT;
   if (dev < kMaxDevices && !g_attr_done[dev][D == 128][G]) {
-    if (cudaFuncSetAttribute(dms::decode_kernel<D, G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) !=
+    if (cudaFuncSetAttribute(dms::decode_kernel<D, G, false, dms::kKvBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) !=
         cudaSuccess) {
       cudaGetLastError();
       return DMS_ERR_CUDA;
@@ -133,7 +133,7 @@ int run(int dev, int num_sms, unsigned char* scratch, const void* k_pool, const 
     cudaGetLastError();
     return DMS_ERR_CUDA;
   }
-  return launch_dependent(dms::decode_kernel<D, G, false>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
+  return launch_dependent(dms::decode_kernel<D, G, false, dms::kKvBf16>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
 }
 
 template <int D>

@@ -24,12 +24,18 @@ DMS_ERR_TIMEOUT = -5
 DMS_ERR_EMPTY = -6
 DMS_ERR_SCRATCH_LIMIT = -7
 DMS_MAX_GROUP = 8
+DMS_KV_BF16 = 0
+DMS_KV_FP8_E4M3 = 1
+KV_FORMATS = {"bf16": DMS_KV_BF16, "fp8": DMS_KV_FP8_E4M3}
 
 # Entry points declared in include/dms.h: name -> (restype, argtypes)
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 SIGNATURES = {
     "dms_cache_create": (_P, [_I, _I, _I, _I, _I]),
+    "dms_cache_create_ex": (_P, [_I, _I, _I, _I, _I, _I]),
+    "dms_cache_kv_format": (_I, [_P]),
+    "dms_cache_export_scales": (_I, [_P, _P, _P, _P]),
     "dms_last_error": (_I, []),
     "dms_cache_destroy": (None, [_P]),
     "dms_append": (_I, [_P, _P, _P, _P, _P]),
@@ -104,17 +110,22 @@ class DmsCache:
     owned by libdms.so)."""
 
     def __init__(self, batch: int, kv_heads: int, capacity: int, head_dim: int, window: int = 16,
-                 device=None):
+                 device=None, kv_format: str = "bf16"):
+        """kv_format: "bf16" (rows stored as given) or "fp8" (E4M3 codes with a
+        float32 scale per row; see dms_cache_create_ex)."""
         self._lib = load_library()
+        if kv_format not in KV_FORMATS:
+            raise ValueError(f"kv_format must be one of {sorted(KV_FORMATS)}")
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None
                                    else torch.device(device).index or 0)
         with torch.cuda.device(self.device):
-            h = self._lib.dms_cache_create(batch, kv_heads, capacity, head_dim, window)
+            h = self._lib.dms_cache_create_ex(batch, kv_heads, capacity, head_dim, window, KV_FORMATS[kv_format])
         if not h:
-            raise DmsError(self._lib.dms_last_error(), "dms_cache_create")
+            raise DmsError(self._lib.dms_last_error(), "dms_cache_create_ex")
         self._h = ctypes.c_void_p(h)
         self.batch, self.kv_heads, self.capacity, self.head_dim, self.window = (
             batch, kv_heads, capacity, head_dim, window)
+        self.kv_format = kv_format
 
     # -- lifetime -----------------------------------------------------------
     def close(self) -> None:
@@ -222,11 +233,23 @@ class DmsCache:
         return out
 
     def export_kv(self, stream=None):
+        """K and V pools in logical order: bf16 rows, or for an fp8 cache the
+        uint8 E4M3 codes (scales: export_scales)."""
         shp = (self.batch, self.kv_heads, self.capacity, self.head_dim)
-        k = torch.empty(shp, dtype=torch.bfloat16, device=self.device)
-        v = torch.empty(shp, dtype=torch.bfloat16, device=self.device)
+        dt = torch.uint8 if self.kv_format == "fp8" else torch.bfloat16
+        k = torch.empty(shp, dtype=dt, device=self.device)
+        v = torch.empty(shp, dtype=dt, device=self.device)
         _check(self._lib.dms_cache_export_kv(self.handle, k.data_ptr(), v.data_ptr(), _stream_handle(stream)),
                "dms_cache_export_kv")
+        return k, v
+
+    def export_scales(self, stream=None):
+        """fp8 caches: the float32 K and V scales of every slot, [B][Hkv][cap] each."""
+        shp = (self.batch, self.kv_heads, self.capacity)
+        k = torch.empty(shp, dtype=torch.float32, device=self.device)
+        v = torch.empty(shp, dtype=torch.float32, device=self.device)
+        _check(self._lib.dms_cache_export_scales(self.handle, k.data_ptr(), v.data_ptr(), _stream_handle(stream)),
+               "dms_cache_export_scales")
         return k, v
 
     def status(self, stream=None) -> int:
@@ -237,6 +260,10 @@ class DmsCache:
 # Module-level aliases carrying the C entry-point names.
 def dms_cache_create(batch, kv_heads, capacity, head_dim, window=16, device=None) -> DmsCache:
     return DmsCache(batch, kv_heads, capacity, head_dim, window, device)
+
+
+def dms_cache_create_ex(batch, kv_heads, capacity, head_dim, window=16, kv_format="bf16", device=None) -> DmsCache:
+    return DmsCache(batch, kv_heads, capacity, head_dim, window, device, kv_format)
 
 
 def dms_append(cache: DmsCache, k, v, evict_logit, stream=None) -> None:

@@ -50,6 +50,9 @@ def test_null_handle_rejected_without_device(lib):
     assert lib.dms_cache_status(None, None) == dms.DMS_ERR_BAD_HANDLE
     assert lib.dms_cache_selftest_wait(None, None) == dms.DMS_ERR_BAD_HANDLE
     assert lib.dms_prefill(None, None, None, None, None, 4, None, 1.0, 4, None) == dms.DMS_ERR_BAD_HANDLE
+    assert lib.dms_cache_export_scales(None, None, None, None) == dms.DMS_ERR_BAD_HANDLE
+    assert lib.dms_cache_kv_format(None) == dms.DMS_ERR_BAD_HANDLE
+    assert lib.dms_step(None, None, None, None, None, None, 1.0, 4, None) == dms.DMS_ERR_BAD_HANDLE
     assert lib.dms_cache_position(None) == -1
     lib.dms_cache_destroy(None)  # ignored
     fake = ctypes.c_void_p(0x1000)  # never returned by dms_cache_create
@@ -60,6 +63,9 @@ def test_create_rejects_bad_sizes(lib):
     for args in [(0, 8, 16, 128, 16), (1, 0, 16, 128, 16), (1, 8, 0, 128, 16), (1, 8, 16, 96, 16),
                  (1, 8, 16, 128, 0), (1 << 16, 1 << 10, 1 << 12, 128, 16)]:
         assert lib.dms_cache_create(*args) is None
+        assert lib.dms_last_error() == dms.DMS_ERR_INVALID_ARG
+    for fmt in (-1, 2, 7):  # unknown storage format
+        assert lib.dms_cache_create_ex(1, 8, 16, 128, 16, fmt) is None
         assert lib.dms_last_error() == dms.DMS_ERR_INVALID_ARG
 
 
