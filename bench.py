@@ -515,6 +515,59 @@ def time_fp8_leg(dms, W, wl, device, steps):
             "note": "step = append kernel + decode kernel (the fused one-launch step is bf16 only)"}
 
 
+def time_graph_leg(dms, W, device, steps):
+    """The long-context stack's decode step over all its layers (one cache per
+    layer, each filled to the stack's prefill length): `steps` steps as one
+    dms_step call per layer, then as one launch of a DmsStepGraph holding the
+    same per-layer steps.  Device time from events around each pass, host time
+    of the enqueue loops from the wall clock."""
+    import time as _time
+    wl = W.WORKLOADS["long-context"]
+    lib = dms.load_library()
+    stream = torch.cuda.current_stream(device)
+    caches = [fill_cache(dms, W, wl, wl.prefill, device, layer=layer) for layer in range(wl.layers)]
+    ins = [step_inputs(W, wl, wl.prefill, 1, device, layer=layer) for layer in range(wl.layers)]
+    qs, ks, vs, ls = ([x[j][0] for x in ins] for j in range(4))
+    outs = [torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device=device) for _ in caches]
+
+    def per_layer_step():
+        for c, k, v, lg, q, o in zip(caches, ks, vs, ls, qs, outs):
+            rc = lib.dms_step(c.handle, k.data_ptr(), v.data_ptr(), lg.data_ptr(), q.data_ptr(), o.data_ptr(),
+                              wl.scale, wl.Hq, stream.cuda_stream)
+            if rc:
+                raise dms.DmsError(rc, "dms_step")
+
+    graph = dms.DmsStepGraph(caches, ks, vs, ls, qs, outs, wl.scale)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h0 = _time.perf_counter()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        h1 = _time.perf_counter()
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) * 1e3 / steps, (h1 - h0) * 1e6 / steps
+
+    dev_loop, host_loop = timed(per_layer_step)
+    dev_graph, host_graph = timed(lambda: graph.launch(stream))
+    graph.close()
+    st = [c.status() for c in caches]
+    for c in caches:
+        c.close()
+    if any(st):
+        raise dms.DmsError(max(st, key=abs), "graph leg")
+    return {"workload": f"long-context stack: {wl.layers} layers, batch {wl.B}, {wl.Hq} query / {wl.Hkv} KV heads, "
+                        f"head_dim {wl.D}, context {wl.prefill}", "layers": wl.layers, "steps": steps,
+            "per_layer_calls": {"us_per_step_device": dev_loop, "us_per_step_host_enqueue": host_loop},
+            "graph": {"us_per_step_device": dev_graph, "us_per_step_host_enqueue": host_graph},
+            "tokens_per_s_graph": wl.B / (dev_graph * 1e-6)}
+
+
 def measured_bf16_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -642,6 +695,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-storage leg")
+    ap.add_argument("--no-graph", action="store_true", help="skip the multi-layer CUDA-graph step leg")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill leg and print its figures (for profiling)")
     ap.add_argument("--prefill-chunks", type=int, default=9)
@@ -764,6 +818,8 @@ def main():
                                "(one copy), append + decode, output copied out, stream synchronized every step"}
     if not args.no_variants and world == 1:
         line["variants"] = time_variants(dms, W, device, 32)
+    if not args.no_graph and world == 1:
+        line["step_graph"] = time_graph_leg(dms, W, device, 32)
     if not args.no_fp8 and world == 1:
         fp8 = time_fp8_leg(dms, W, wl, device, 64)
         fp8["decode_speedup_over_bf16"] = r["decode_us"] / fp8["decode_us_per_launch_back_to_back"]

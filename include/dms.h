@@ -202,6 +202,41 @@ int dms_cache_status(dms_cache_t* cache, void* stream);
  * no counterpart; this exists to test error reporting.) */
 int dms_cache_selftest_wait(dms_cache_t* cache, void* stream);
 
+/*
+ * A decode step over several caches (the layers of a model, say) captured
+ * once into a CUDA graph and replayed per token, so that a step costs one
+ * graph launch instead of one library call per layer.
+ *
+ * dms_step_graph_create captures, for i = 0 .. n-1, the fused step of
+ * dms_step on caches[i] with the caller's buffers k[i], v[i], evict_logit[i],
+ * q[i], out[i] (layouts as for dms_step; device memory, 16-byte aligned), the
+ * given scale and q_heads; then one node that advances every cache's
+ * position.  The buffers are bound by address: before each launch the caller
+ * writes that step's inputs into them, and after it reads out[i].  The caches
+ * must be distinct bf16 caches on one device; the graph does not own them and
+ * must be destroyed before they are.  Returns NULL on failure (dms_last_error()
+ * gives the code; stream capture must not be active on the calling thread).
+ *
+ * dms_step_graph_launch enqueues one step on `stream`: the result equals
+ * dms_step on every cache in order, bit for bit.  Each cache's position is
+ * also kept in device memory, which the replayed kernels read; if a cache
+ * advanced outside the graph since the last launch (dms_append, dms_step, ...)
+ * a one-thread kernel first re-sends its position.  The host counters advance
+ * by one.  No allocation.
+ *
+ * Method reference: the step is the method's decode (append with delayed
+ * eviction, then attention over the retained cache), "Inference-Time
+ * Hyper-Scaling with KV Cache Compression", AI research-map summary,
+ * "Approach"; the graph only changes how it is launched.
+ */
+typedef struct dms_step_graph dms_step_graph_t;
+dms_step_graph_t* dms_step_graph_create(dms_cache_t* const* caches, int n, const void* const* k,
+                                        const void* const* v, const float* const* evict_logit,
+                                        const void* const* q, float* const* out, float scale, int q_heads);
+int dms_step_graph_launch(dms_step_graph_t* graph, void* stream);
+/* Synchronizes the device, then frees the graph.  NULL is ignored. */
+void dms_step_graph_destroy(dms_step_graph_t* graph);
+
 /* Number of tokens appended so far (the host position counter t), or -1. */
 int64_t dms_cache_position(dms_cache_t* cache);
 

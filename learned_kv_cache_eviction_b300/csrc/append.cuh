@@ -272,4 +272,17 @@ __global__ void export_scales_kernel(CacheView c, float* __restrict__ k_scale, f
   }
 }
 
+// Positions of caches whose steps are replayed from a CUDA graph: the last
+// node of the graph advances each cache's position word by one, and a launch
+// after calls made outside the graph first re-sends the host's position.
+__global__ void advance_positions_kernel(int64_t* const* __restrict__ pos, int n) {
+  griddep_wait();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) *pos[i] += 1;
+}
+
+__global__ void set_position_kernel(int64_t* pos, int64_t value) {
+  griddep_wait();
+  *pos = value;
+}
+
 }  // namespace dms

@@ -70,9 +70,11 @@ struct DecodeShape {
   static constexpr int OFF_BAR = OFF_P + TK * PROW * 4;
   // Fused step: per-warp state kept in shared memory rather than in registers
   // (the decode loop has none to spare): the new token's slots of the first
-  // FX_HEADS heads of the warp's range, the first head, the current segment's.
-  static constexpr int FX_HEADS = 14;
+  // FX_HEADS heads of the warp's range, the first head, the current segment's,
+  // and the step's position.
+  static constexpr int FX_HEADS = 12;
   static constexpr int FX_I0 = FX_HEADS, FX_SEG = FX_HEADS + 1;
+  static constexpr int FX_T = FX_HEADS + 2;  // the step's position t (int64, two slots)
   static constexpr int OFF_FX = OFF_BAR + NST * 8;
   static constexpr int FX_BYTES = FP8 ? 0 : (FX_HEADS + 2) * 4;  // the fused step is bf16 only
   static constexpr int WARP_BYTES = ((OFF_FX + FX_BYTES + 127) / 128) * 128;
@@ -108,10 +110,12 @@ struct DecodeArgs {
   int NH, Hkv, cap;
   float qscale;  // scale * log2(e)
   // Fused step only (decode_kernel<D, G, true>, dms_step): the new token of
-  // position t is appended in the same launch.  `len` then holds the lengths
-  // before it; the kernel decodes over the lengths after it and writes those,
-  // the token's ring entry, slot map entry and K/V row into the other halves
-  // of the double-buffered state (see CacheView), which no CTA reads.
+  // position t is appended in the same launch.  `len` is then the base of the
+  // double-buffered lengths [2][NH] (see CacheView): the kernel decodes over
+  // the lengths after the token and writes those, the token's ring entry, slot
+  // map entry and K/V row into the other halves of the double-buffered state,
+  // which no CTA reads.  The position t comes from `t`, or, when t_dev is set
+  // (a step replayed from a CUDA graph), from device memory.
   const uint4* k_new;     // [NH][D/8] the new token's K and V
   const uint4* v_new;
   const float* logit_new;  // [NH]
@@ -120,26 +124,28 @@ struct DecodeArgs {
   int32_t* slot_pos;      // [NH][cap]
   int32_t* ring_slot;     // [2][NH][w]
   uint8_t* ring_flag;     // [2][NH][w]
-  int32_t* len_new;       // [NH] lengths after the append
+  int32_t* len_w;         // [2][NH] the lengths, writable
+  const int64_t* t_dev;   // graph-replayed steps: the cache's position in device memory
   int64_t t;
   int w;
 };
 
-// The new token's slot in head x for the fused step: the slot of token t - w if
-// that token was stored and marked (it leaves now), else the next free slot,
-// else -1 (capacity exceeded).  Reads only the state before the step.
-__device__ __forceinline__ int fused_new_slot(const DecodeArgs& a, int x, int L_old) {
-  if (a.t >= a.w) {
-    const size_t e = ring_index(a.NH, a.w, x, a.t - a.w);
+// The new token's slot in head x for the fused step at position t: the slot of
+// token t - w if that token was stored and marked (it leaves now), else the
+// next free slot, else -1 (capacity exceeded).  Reads only the state before
+// the step.
+__device__ __forceinline__ int fused_new_slot(const DecodeArgs& a, int64_t t, int x, int L_old) {
+  if (t >= a.w) {
+    const size_t e = ring_index(a.NH, a.w, x, t - a.w);
     if (a.ring_flag[e]) return a.ring_slot[e];
   }
   return L_old < a.cap ? L_old : -1;
 }
 
-// Not inlined: the slot lookup of a head beyond the first 32 of a warp's range
-// (rare), kept out of the decode loop's code.
-static __device__ __noinline__ int fused_new_slot_far(const DecodeArgs& a, int x) {
-  return fused_new_slot(a, x, a.len[x]);
+// Not inlined: the slot lookup of a head beyond the first FX_HEADS of a warp's
+// range (rare), kept out of the decode loop's code.
+static __device__ __noinline__ int fused_new_slot_far(const DecodeArgs& a, int64_t t, int x) {
+  return fused_new_slot(a, t, x, a.len[(t & 1) * a.NH + x]);
 }
 
 // Fused step, not inlined (once per head, in the warp whose tile holds the new
@@ -159,15 +165,16 @@ static __device__ __noinline__ void patch_new_row(const DecodeArgs& a, uint4* Kt
   __syncwarp();
 }
 
-// Retained length of head x as this launch decodes it.
+// Retained length of head x as this launch decodes it (fused: after the
+// append of position t).
 template <bool FUSED>
-__device__ __forceinline__ int decode_len(const DecodeArgs& a, int x) {
-  const int L = a.len[x];
+__device__ __forceinline__ int decode_len(const DecodeArgs& a, int64_t t, int x) {
   if constexpr (FUSED) {
-    const bool retire = a.t >= a.w && a.ring_flag[ring_index(a.NH, a.w, x, a.t - a.w)] != 0;
+    const int L = a.len[(t & 1) * a.NH + x];
+    const bool retire = t >= a.w && a.ring_flag[ring_index(a.NH, a.w, x, t - a.w)] != 0;
     return (!retire && L < a.cap) ? L + 1 : L;
   }
-  return L;
+  return a.len[x];
 }
 
 // Retained-slot iterator over one warp's global range [A, E).
@@ -357,7 +364,12 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   const int wl = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t wg = static_cast<int64_t>(blockIdx.x) * NW + wl;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * NW;
-  auto lenf = [&](int x) { return decode_len<FUSED>(a, x); };
+  // The step's position (fused step only): a kernel argument, or read from
+  // device memory when the launch is replayed from a CUDA graph.
+  int64_t t_step = a.t;
+  if constexpr (FUSED) {
+    if (a.t_dev != nullptr) t_step = __ldcg(a.t_dev);
+  }
   int* pre = reinterpret_cast<int*>(smem);  // [NH + 1]; aliases the warp regions until the barrier below
   int* sn = pre + a.NH + 1;                 // fused step: [NH] the new token's slot in each head
   // Fused step: warp x of the grid appends the token to head x (and x + nwarps,
@@ -376,10 +388,10 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   // the fused scan also records the new token's slot in sn.
   auto scanf = [&](int x) {
     if constexpr (FUSED) {
-      const int L = a.len[x];
+      const int L = a.len[(t_step & 1) * a.NH + x];
       int fl = 0, sl = 0;
-      if (a.t >= a.w) {
-        const size_t e = ring_index(a.NH, a.w, x, a.t - a.w);
+      if (t_step >= a.w) {
+        const size_t e = ring_index(a.NH, a.w, x, t_step - a.w);
         fl = a.ring_flag[e];
         sl = a.ring_slot[e];
       }
@@ -404,11 +416,11 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
         lg = __ldg(a.logit_new + i);
       }
       if (lane == 0) {
-        a.len_new[i] = pre[i + 1] - pre[i];
-        const size_t e = ring_index(a.NH, a.w, i, a.t);
+        a.len_w[((t_step + 1) & 1) * a.NH + i] = pre[i + 1] - pre[i];
+        const size_t e = ring_index(a.NH, a.w, i, t_step);
         a.ring_slot[e] = s_new;
         a.ring_flag[e] = (s_new >= 0 && lg > 0.0f) ? 1 : 0;
-        if (s_new >= 0) a.slot_pos[static_cast<size_t>(i) * a.cap + s_new] = static_cast<int32_t>(a.t);
+        if (s_new >= 0) a.slot_pos[static_cast<size_t>(i) * a.cap + s_new] = static_cast<int32_t>(t_step);
         else atomicOr(a.err, kErrBitCapacity);
       }
       if (s_new >= 0) {
@@ -463,9 +475,16 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
     if (lane == 0) {
       fx[Sh::FX_I0] = i0;
       fx[Sh::FX_SEG] = -1;
+      *reinterpret_cast<int64_t*>(fx + Sh::FX_T) = t_step;
     }
   }
   __syncwarp();
+  // Retained length of head x after this launch's append (read per head
+  // change; the position comes from shared memory, not a register).
+  auto lenf = [&](int x) {
+    if constexpr (FUSED) return decode_len<true>(a, *reinterpret_cast<const int64_t*>(fx + Sh::FX_T), x);
+    else return decode_len<false>(a, 0, x);
+  };
 
   const int Hq = a.Hkv * G;
   TileIter is, cs;
@@ -551,7 +570,8 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
       seg_P = cs.P;
       if constexpr (FUSED) {
         const int d = cs.i - fx[Sh::FX_I0];
-        const int sw = d < Sh::FX_HEADS ? fx[d] : fused_new_slot_far(a, cs.i);
+        const int sw =
+            d < Sh::FX_HEADS ? fx[d] : fused_new_slot_far(a, *reinterpret_cast<const int64_t*>(fx + Sh::FX_T), cs.i);
         __syncwarp();
         if (lane == 0) fx[Sh::FX_SEG] = sw;
         __syncwarp();

@@ -10,6 +10,7 @@
 #include <mutex>
 #include <new>
 #include <unordered_set>
+#include <vector>
 #include <utility>
 
 #include "append.cuh"
@@ -28,6 +29,11 @@ struct dms_cache {
   float* part_ml;
   int32_t* head_cnt;  // [NH] arrival counters of heads split across warps (zero between calls)
   size_t part_entries;
+  // The position in device memory, read by steps replayed from a CUDA graph
+  // (dms_step_graph_*).  Valid while t_dev_synced; any call that advances t
+  // outside a graph clears the flag, and the next graph launch re-sends t.
+  int64_t* t_dev;
+  bool t_dev_synced;
 };
 
 namespace {
@@ -98,31 +104,47 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
   return launch_status();
 }
 
-// The new token of a fused step (dms_step): its K, V rows and eviction logit.
+// The new token of a fused step (dms_step): its K, V rows and eviction logit;
+// t_dev set when the launch is captured into a CUDA graph (the position is
+// then read from device memory at replay).
 struct StepInput {
   const uint4* k;
   const uint4* v;
   const float* logit;
+  const int64_t* t_dev;
 };
 
 // Decode launch.  Plain (FUSED false): attention of q over the cache as it
 // stands at position c->t.  Fused (FUSED true, `in` set): the token of
 // position c->t is appended in the same launch and the attention runs over
 // the cache after it; the caller then advances c->t.
+// Opt the decode kernel into its dynamic shared memory on c's device (once;
+// not a stream operation, so it is done before any stream capture).
+template <int D, int G, bool FUSED, int KVF>
+int decode_attr(const dms_cache* c) {
+  using Sh = dms::DecodeShape<D, G, KVF>;
+  static bool attr_done[64] = {};
+  if (c->device < 64 && attr_done[c->device]) return DMS_OK;
+  if (cudaFuncSetAttribute(dms::decode_kernel<D, G, FUSED, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Sh::SMEM) != cudaSuccess) {
+    cudaGetLastError();
+    return DMS_ERR_CUDA;
+  }
+  if (c->device < 64) attr_done[c->device] = true;
+  return DMS_OK;
+}
+
 template <int D, int G, bool FUSED, int KVF>
 int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaStream_t st, const StepInput* in) {
   using Sh = dms::DecodeShape<D, G, KVF>;
-  static bool attr_done[64] = {};
-  if (c->device < 64 && !attr_done[c->device]) {
-    if (cudaFuncSetAttribute(dms::decode_kernel<D, G, FUSED, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Sh::SMEM) != cudaSuccess)
-      return DMS_ERR_CUDA;
-    attr_done[c->device] = true;
-  }
+  if (decode_attr<D, G, FUSED, KVF>(c) != DMS_OK) return DMS_ERR_CUDA;
   // The prologue's prefix sums (and, fused, each head's new slot) fit in shared memory.
   if (static_cast<int64_t>((FUSED ? 2 : 1) * c->NH + 1) * 4 > Sh::SMEM) return DMS_ERR_INVALID_ARG;
-  // Upper bound of the retained slots (the exact sum lives on the device).
-  const int64_t smax = static_cast<int64_t>(c->NH) * std::min<int64_t>(c->t + (FUSED ? 1 : 0), c->cap);
+  // Upper bound of the retained slots (the exact sum lives on the device); a
+  // graph-replayed step runs at positions unknown now, so it takes the capacity.
+  const bool graph = FUSED && in != nullptr && in->t_dev != nullptr;
+  const int64_t smax =
+      static_cast<int64_t>(c->NH) * (graph ? c->cap : std::min<int64_t>(c->t + (FUSED ? 1 : 0), c->cap));
   const int64_t want = (smax + int64_t(dms::kMinSlotsPerWarp) * Sh::NW - 1) / (int64_t(dms::kMinSlotsPerWarp) * Sh::NW);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(c->num_sms, want)));
   if (static_cast<size_t>(grid) * Sh::NW + c->NH > c->part_entries) return DMS_ERR_INVALID_ARG;
@@ -148,7 +170,8 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
   a.slot_pos = nullptr;
   a.ring_slot = c->view.ring_slot;
   a.ring_flag = c->view.ring_flag;
-  a.len_new = nullptr;
+  a.len_w = nullptr;
+  a.t_dev = nullptr;
   a.t = c->t;
   a.w = c->w;
   if constexpr (FUSED) {
@@ -158,7 +181,9 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
     a.K_w = c->view.K;
     a.V_w = c->view.V;
     a.slot_pos = c->view.slot_pos;
-    a.len_new = dms::len_after(c->view, c->t + 1);
+    a.len = c->view.len;  // both halves: the kernel picks them by the position's parity
+    a.len_w = c->view.len;
+    a.t_dev = in->t_dev;
   }
   return launch_pdl(dms::decode_kernel<D, G, FUSED, KVF>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
 }
@@ -216,6 +241,22 @@ int launch_prefill_d(dms_cache* c, const dms::PrefillArgs& a, int G, cudaStream_
   }
 }
 
+// decode_attr for the cache's head dim and group size (fused kernel).
+template <int D>
+int fused_attr_d(const dms_cache* c, int G) {
+  switch (G) {
+    case 1: return decode_attr<D, 1, true, dms::kKvBf16>(c);
+    case 2: return decode_attr<D, 2, true, dms::kKvBf16>(c);
+    case 3: return decode_attr<D, 3, true, dms::kKvBf16>(c);
+    case 4: return decode_attr<D, 4, true, dms::kKvBf16>(c);
+    case 5: return decode_attr<D, 5, true, dms::kKvBf16>(c);
+    case 6: return decode_attr<D, 6, true, dms::kKvBf16>(c);
+    case 7: return decode_attr<D, 7, true, dms::kKvBf16>(c);
+    case 8: return decode_attr<D, 8, true, dms::kKvBf16>(c);
+    default: return DMS_ERR_INVALID_ARG;
+  }
+}
+
 // Decode launch for the cache's storage format.
 template <int D, bool FUSED>
 int launch_decode_f(dms_cache* c, const void* q, float* out, float scale, int G, cudaStream_t st,
@@ -260,6 +301,19 @@ int launch_append_chunk(dms_cache* c, const void* k, const void* v, const float*
              : launch_pdl(dms::append_chunk_copy_kernel<64, dms::kKvBf16>, grid, dim3(256), 0, st, c->view, k4, v4,
                           c->t, chunk);
 }
+
+}  // namespace
+
+// A decode step over several caches captured into a CUDA graph.
+struct dms_step_graph {
+  std::vector<dms_cache*> caches;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int64_t** pos = nullptr;  // device array: each cache's position word
+  int device = 0;
+};
+
+namespace {
 
 void free_cache_memory(dms_cache* c) {
   cudaFree(c->view.K);
@@ -366,6 +420,8 @@ dms_cache_t* dms_cache_create_ex(int batch, int kv_heads, int capacity, int head
   c->view.D = head_dim;
   c->view.w = window;
   c->view.kvf = fp8 ? dms::kKvFp8 : dms::kKvBf16;
+  c->t_dev = reinterpret_cast<int64_t*>(reinterpret_cast<char*>(c->view.err) + 64);  // zeroed with the error word
+  c->t_dev_synced = true;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     g_live.insert(c);
@@ -397,6 +453,7 @@ int dms_append(dms_cache_t* c, const void* k, const void* v, const float* evict_
     return DMS_ERR_INVALID_ARG;
   const int rc = launch_append(c, k, v, evict_logit, static_cast<cudaStream_t>(stream));
   if (rc == DMS_OK) c->t += 1;
+  c->t_dev_synced = false;
   return rc;
 }
 
@@ -410,6 +467,7 @@ int dms_append_chunk(dms_cache_t* c, const void* k, const void* v, const float* 
     return DMS_ERR_INVALID_ARG;
   const int rc = launch_append_chunk(c, k, v, logits, chunk, static_cast<cudaStream_t>(stream));
   if (rc == DMS_OK) c->t += chunk;
+  c->t_dev_synced = false;
   return rc;
 }
 
@@ -451,6 +509,7 @@ int dms_prefill(dms_cache_t* c, const void* q, const void* k, const void* v, con
   if (rc != DMS_OK) return rc;
   rc = launch_append_chunk(c, k, v, logits, chunk, st);
   if (rc == DMS_OK) c->t += chunk;
+  c->t_dev_synced = false;
   return rc;
 }
 
@@ -489,17 +548,19 @@ int dms_step(dms_cache_t* c, const void* k, const void* v, const float* evict_lo
     int rc = launch_append(c, k, v, evict_logit, st);
     if (rc != DMS_OK) return rc;
     c->t += 1;
+    c->t_dev_synced = false;
     return c->D == 128 ? launch_decode_f<128, false>(c, q, out, scale, G, st)
                        : launch_decode_f<64, false>(c, q, out, scale, G, st);
   }
   // bf16: one launch.  The decode kernel appends the token (into the halves of
   // the double-buffered state that the step does not read) and attends over
   // the cache after the append.
-  const StepInput in{static_cast<const uint4*>(k), static_cast<const uint4*>(v), evict_logit};
+  const StepInput in{static_cast<const uint4*>(k), static_cast<const uint4*>(v), evict_logit, nullptr};
   const int rc = c->D == 128 ? launch_decode_f<128, true>(c, q, out, scale, G, st, &in)
                              : launch_decode_f<64, true>(c, q, out, scale, G, st, &in);
   if (rc != DMS_OK) return rc;
   c->t += 1;
+  c->t_dev_synced = false;
   return DMS_OK;
 }
 
@@ -578,6 +639,113 @@ int dms_cache_status(dms_cache_t* c, void* stream) {
   if (bits & dms::kErrBitTimeout) return DMS_ERR_TIMEOUT;
   if (bits & dms::kErrBitCapacity) return DMS_ERR_CAPACITY;
   return DMS_OK;
+}
+
+dms_step_graph_t* dms_step_graph_create(dms_cache_t* const* caches, int n, const void* const* k,
+                                        const void* const* v, const float* const* evict_logit,
+                                        const void* const* q, float* const* out, float scale, int q_heads) {
+  g_last_error = DMS_ERR_INVALID_ARG;
+  if (n < 1 || !caches || !k || !v || !evict_logit || !q || !out || !std::isfinite(scale) || q_heads < 1)
+    return nullptr;
+  std::unordered_set<const dms_cache*> seen;
+  for (int i = 0; i < n; ++i) {
+    dms_cache* c = caches[i];
+    if (!is_live(c)) {
+      g_last_error = DMS_ERR_BAD_HANDLE;
+      return nullptr;
+    }
+    if (!seen.insert(c).second || c->kvf != DMS_KV_BF16 || c->device != caches[0]->device ||
+        q_heads % c->H != 0 || q_heads / c->H > DMS_MAX_GROUP || !k[i] || !v[i] || !evict_logit[i] || !q[i] ||
+        !out[i] || !aligned16(k[i]) || !aligned16(v[i]) || !aligned16(evict_logit[i]) || !aligned16(q[i]) ||
+        !aligned16(out[i]))
+      return nullptr;
+  }
+  DeviceGuard g(caches[0]->device);
+  g_last_error = DMS_ERR_CUDA;
+  if (!g.ok) return nullptr;
+  for (int i = 0; i < n; ++i) {
+    dms_cache* c = caches[i];
+    if (!device_pointer_ok(k[i], c->device) || !device_pointer_ok(v[i], c->device) ||
+        !device_pointer_ok(evict_logit[i], c->device) || !device_pointer_ok(q[i], c->device) ||
+        !device_pointer_ok(out[i], c->device)) {
+      g_last_error = DMS_ERR_INVALID_ARG;
+      return nullptr;
+    }
+    const int G = q_heads / c->H;
+    if ((c->D == 128 ? fused_attr_d<128>(c, G) : fused_attr_d<64>(c, G)) != DMS_OK) return nullptr;
+  }
+  dms_step_graph* sg = new (std::nothrow) dms_step_graph();
+  if (!sg) return nullptr;
+  sg->device = caches[0]->device;
+  sg->caches.assign(caches, caches + n);
+  std::vector<int64_t*> pos(n);
+  for (int i = 0; i < n; ++i) pos[i] = caches[i]->t_dev;
+  cudaStream_t st = nullptr;
+  bool ok = cudaMalloc(&sg->pos, n * sizeof(int64_t*)) == cudaSuccess &&
+            cudaMemcpy(sg->pos, pos.data(), n * sizeof(int64_t*), cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+  int rc = DMS_OK;
+  if (ok) {
+    // One fused step per cache, each reading its position from device memory,
+    // then one node that advances every position.
+    for (int i = 0; i < n && rc == DMS_OK; ++i) {
+      dms_cache* c = caches[i];
+      const StepInput in{static_cast<const uint4*>(k[i]), static_cast<const uint4*>(v[i]), evict_logit[i], c->t_dev};
+      const int G = q_heads / c->H;
+      rc = c->D == 128 ? launch_decode_d<128, true, dms::kKvBf16>(c, q[i], out[i], scale, G, st, &in)
+                       : launch_decode_d<64, true, dms::kKvBf16>(c, q[i], out[i], scale, G, st, &in);
+    }
+    if (rc == DMS_OK) rc = launch_pdl(dms::advance_positions_kernel, dim3(1), dim3(32), 0, st, sg->pos, n);
+    cudaGraph_t graph = nullptr;
+    const bool ended = cudaStreamEndCapture(st, &graph) == cudaSuccess;
+    sg->graph = graph;
+    ok = rc == DMS_OK && ended && graph != nullptr &&
+         cudaGraphInstantiate(&sg->exec, graph, 0) == cudaSuccess;
+  }
+  if (st) cudaStreamDestroy(st);
+  if (!ok) {
+    cudaGetLastError();
+    if (sg->exec) cudaGraphExecDestroy(sg->exec);
+    if (sg->graph) cudaGraphDestroy(sg->graph);
+    cudaFree(sg->pos);
+    delete sg;
+    g_last_error = rc == DMS_ERR_INVALID_ARG ? DMS_ERR_INVALID_ARG : DMS_ERR_CUDA;
+    return nullptr;
+  }
+  g_last_error = DMS_OK;
+  return sg;
+}
+
+int dms_step_graph_launch(dms_step_graph_t* sg, void* stream) {
+  if (!sg) return DMS_ERR_BAD_HANDLE;
+  for (dms_cache* c : sg->caches)
+    if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  DeviceGuard g(sg->device);
+  if (!g.ok) return DMS_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (dms_cache* c : sg->caches) {
+    if (c->t_dev_synced) continue;
+    const int rc = launch_pdl(dms::set_position_kernel, dim3(1), dim3(1), 0, st, c->t_dev, c->t);
+    if (rc != DMS_OK) return rc;
+    c->t_dev_synced = true;
+  }
+  if (cudaGraphLaunch(sg->exec, st) != cudaSuccess) {
+    cudaGetLastError();
+    return DMS_ERR_CUDA;
+  }
+  for (dms_cache* c : sg->caches) c->t += 1;
+  return DMS_OK;
+}
+
+void dms_step_graph_destroy(dms_step_graph_t* sg) {
+  if (!sg) return;
+  DeviceGuard g(sg->device);
+  cudaDeviceSynchronize();
+  if (sg->exec) cudaGraphExecDestroy(sg->exec);
+  if (sg->graph) cudaGraphDestroy(sg->graph);
+  cudaFree(sg->pos);
+  delete sg;
 }
 
 }  // extern "C"

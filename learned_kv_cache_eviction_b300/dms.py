@@ -36,6 +36,9 @@ SIGNATURES = {
     "dms_cache_create_ex": (_P, [_I, _I, _I, _I, _I, _I]),
     "dms_cache_kv_format": (_I, [_P]),
     "dms_cache_export_scales": (_I, [_P, _P, _P, _P]),
+    "dms_step_graph_create": (_P, [_P, _I, _P, _P, _P, _P, _P, ctypes.c_float, _I]),
+    "dms_step_graph_launch": (_I, [_P, _P]),
+    "dms_step_graph_destroy": (None, [_P]),
     "dms_last_error": (_I, []),
     "dms_cache_destroy": (None, [_P]),
     "dms_append": (_I, [_P, _P, _P, _P, _P]),
@@ -255,6 +258,52 @@ class DmsCache:
     def status(self, stream=None) -> int:
         """Synchronize the stream and return the sticky device status code."""
         return int(self._lib.dms_cache_status(self.handle, _stream_handle(stream)))
+
+
+class DmsStepGraph:
+    """A decode step over several caches (e.g. a model's layers) captured into
+    a CUDA graph (dms_step_graph_create).  The tensors are bound by address:
+    write each step's inputs into them, call launch(), read `out`."""
+
+    def __init__(self, caches, k, v, evict_logit, q, out, scale: float):
+        self._lib = load_library()
+        n = len(caches)
+        if not (n == len(k) == len(v) == len(evict_logit) == len(q) == len(out)) or n == 0:
+            raise ValueError("one k, v, evict_logit, q, out per cache")
+        q_heads = q[0].shape[1]
+        for c, ki, vi, li, qi, oi in zip(caches, k, v, evict_logit, q, out):
+            B, H, D = c.batch, c.kv_heads, c.head_dim
+            _need(ki, "k", torch.bfloat16, (B, H, D), c.device)
+            _need(vi, "v", torch.bfloat16, (B, H, D), c.device)
+            _need(li, "evict_logit", torch.float32, (B, H), c.device)
+            _need(qi, "q", torch.bfloat16, (B, q_heads, D), c.device)
+            _need(oi, "out", torch.float32, (B, q_heads, D), c.device)
+
+        def arr(ts):
+            return (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])
+
+        handles = (ctypes.c_void_p * n)(*[c.handle.value for c in caches])
+        self._keep = (caches, k, v, evict_logit, q, out)
+        with torch.cuda.device(caches[0].device):
+            h = self._lib.dms_step_graph_create(handles, n, arr(k), arr(v), arr(evict_logit), arr(q), arr(out),
+                                                float(scale), q_heads)
+        if not h:
+            raise DmsError(self._lib.dms_last_error(), "dms_step_graph_create")
+        self._h = ctypes.c_void_p(h)
+
+    def launch(self, stream=None) -> None:
+        _check(self._lib.dms_step_graph_launch(self._h, _stream_handle(stream)), "dms_step_graph_launch")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.dms_step_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 # Module-level aliases carrying the C entry-point names.

@@ -433,3 +433,73 @@ def test_variant_workloads_sampled(name, T):
     bookkeeping of all rows bit-exact, outputs of rows {0, 3}."""
     wl = W.WORKLOADS[name].with_(B=4, cap=T + 4)
     _prefill_then_decode(wl, T, 4, rows=[0, wl.B - 1])
+
+
+def test_step_graph_equals_dms_step_per_layer():
+    """A 3-layer decode step captured into a CUDA graph and replayed per token
+    gives the same outputs and cache state, bit for bit, as dms_step on each
+    layer's cache.  Between replays one layer also advances outside the graph
+    (dms_append + dms_decode_attention on both sides), which the next replay
+    must pick up from the host's position."""
+    wl = _small("graph", 2, 8, 2, 128, 16, 300, ("normal", 0.6, 1.0), seed=17)
+    L, T0, T = 3, 40, 120
+    data = [tuple(x.cuda() for x in W.kv_range(wl, layer, 0, T)) + (W.q_range(wl, layer, 0, T).cuda(),)
+            for layer in range(L)]
+    ref = [dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w) for _ in range(L)]
+    got = [dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w) for _ in range(L)]
+    for layer in range(L):
+        k, v, lg, _ = data[layer]
+        for c in (ref[layer], got[layer]):
+            c.append_chunk(k[:, :, :T0].contiguous(), v[:, :, :T0].contiguous(), lg[:, :, :T0].contiguous())
+    kb = [torch.empty((wl.B, wl.Hkv, wl.D), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    vb = [torch.empty_like(x) for x in kb]
+    lb = [torch.empty((wl.B, wl.Hkv), dtype=torch.float32, device="cuda") for _ in range(L)]
+    qb = [torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    ob = [torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda") for _ in range(L)]
+    graph = dms.DmsStepGraph(got, kb, vb, lb, qb, ob, wl.scale)
+    out_ref = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    t = T0
+    while t < T:
+        if t % 25 == 0:  # layer 1 advances outside the graph (both sides)
+            k, v, lg, q = data[1]
+            for c in (ref[1], got[1]):
+                c.append(k[:, :, t].contiguous(), v[:, :, t].contiguous(), lg[:, :, t].contiguous())
+            # keep the layers' positions aligned with their inputs: the other
+            # layers take the same token through their own dms_step
+            for layer in (0, 2):
+                k, v, lg, q = data[layer]
+                for c in (ref[layer], got[layer]):
+                    c.step(k[:, :, t].contiguous(), v[:, :, t].contiguous(), lg[:, :, t].contiguous(),
+                           q[:, :, t].contiguous(), out_ref, scale=wl.scale)
+            t += 1
+            continue
+        for layer in range(L):
+            k, v, lg, q = data[layer]
+            kb[layer].copy_(k[:, :, t])
+            vb[layer].copy_(v[:, :, t])
+            lb[layer].copy_(lg[:, :, t])
+            qb[layer].copy_(q[:, :, t])
+        graph.launch()
+        for layer in range(L):
+            k, v, lg, q = data[layer]
+            ref[layer].step(k[:, :, t].contiguous(), v[:, :, t].contiguous(), lg[:, :, t].contiguous(),
+                            q[:, :, t].contiguous(), out_ref, scale=wl.scale)
+            assert torch.equal(ob[layer], out_ref), (t, layer)
+        t += 1
+    for layer in range(L):
+        assert got[layer].position == ref[layer].position == T
+        assert torch.equal(got[layer].lengths(), ref[layer].lengths())
+        assert torch.equal(got[layer].slot_positions(), ref[layer].slot_positions())
+        ka, va = got[layer].export_kv()
+        kr, vr = ref[layer].export_kv()
+        assert torch.equal(ka, kr) and torch.equal(va, vr)
+        assert got[layer].status() == dms.DMS_OK
+    graph.close()
+    # refused: an fp8 cache, a cache listed twice
+    f = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w, kv_format="fp8")
+    with pytest.raises(dms.DmsError):
+        dms.DmsStepGraph([f], kb[:1], vb[:1], lb[:1], qb[:1], ob[:1], wl.scale)
+    with pytest.raises(dms.DmsError):
+        dms.DmsStepGraph([got[0], got[0]], kb[:2], vb[:2], lb[:2], qb[:2], ob[:2], wl.scale)
+    for c in ref + got + [f]:
+        c.close()

@@ -53,6 +53,10 @@ def test_null_handle_rejected_without_device(lib):
     assert lib.dms_cache_export_scales(None, None, None, None) == dms.DMS_ERR_BAD_HANDLE
     assert lib.dms_cache_kv_format(None) == dms.DMS_ERR_BAD_HANDLE
     assert lib.dms_step(None, None, None, None, None, None, 1.0, 4, None) == dms.DMS_ERR_BAD_HANDLE
+    assert lib.dms_step_graph_launch(None, None) == dms.DMS_ERR_BAD_HANDLE
+    assert lib.dms_step_graph_create(None, 0, None, None, None, None, None, 1.0, 4) is None
+    assert lib.dms_last_error() == dms.DMS_ERR_INVALID_ARG
+    lib.dms_step_graph_destroy(None)  # ignored
     assert lib.dms_cache_position(None) == -1
     lib.dms_cache_destroy(None)  # ignored
     fake = ctypes.c_void_p(0x1000)  # never returned by dms_cache_create
