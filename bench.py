@@ -456,6 +456,72 @@ def time_variants(dms, W, device, steps):
     return rows
 
 
+def time_workloads(dms, W, device, steps):
+    """Decode throughput on every configured workload at its own shapes: the
+    cache (one layer) is filled to the workload's final context (minus the
+    timed steps), then `steps` dms_step calls (append + decode, one fused
+    launch) and `steps` back-to-back dms_decode_attention calls, events around
+    each pass.  Reported per workload: tokens/s of the step, the decode
+    kernel's time, its algorithmic GB/s and fraction of the measured copy
+    bandwidth."""
+    lib = dms.load_library()
+    stream = torch.cuda.current_stream(device)
+    peak, _ = measured_hbm_peak()
+    rows = []
+    for name in ("tiny", "llama-3.2-1b", "qwen3-8b", "qwen-r1-32b", "long-context"):
+        wl = W.WORKLOADS[name]
+        n_end = wl.cap if name != "llama-3.2-1b" else wl.prefill + wl.decode
+        n_end = min(n_end, wl.cap)
+        n0 = n_end - steps - 3
+        cache = fill_cache(dms, W, wl, n0, device)
+        qs, ks, vs, ls = step_inputs(W, wl, n0, steps + 3, device)
+        out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device=device)
+
+        def step(i):
+            rc = lib.dms_step(cache.handle, ks[i].data_ptr(), vs[i].data_ptr(), ls[i].data_ptr(), qs[i].data_ptr(),
+                              out.data_ptr(), wl.scale, wl.Hq, stream.cuda_stream)
+            if rc:
+                raise dms.DmsError(rc, f"dms_step ({name})")
+
+        for i in range(3):
+            step(i)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(3, steps + 3):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        step_us = e0.elapsed_time(e1) * 1e3 / steps
+        len_sum = int(cache.lengths().sum())
+        def decode():
+            rc = lib.dms_decode_attention(cache.handle, qs[-1].data_ptr(), out.data_ptr(), wl.scale, wl.Hq,
+                                          stream.cuda_stream)
+            if rc:
+                raise dms.DmsError(rc, f"dms_decode_attention ({name})")
+
+        for _ in range(8):
+            decode()
+        e0.record(stream)
+        for _ in range(steps):
+            decode()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        dec_us = e0.elapsed_time(e1) * 1e3 / steps
+        st = cache.status()
+        cache.close()
+        if st != dms.DMS_OK:
+            raise dms.DmsError(st, name)
+        gbs = decode_bytes(wl, len_sum) / (dec_us * 1e-6) / 1e9
+        rows.append({"workload": name, "batch": wl.B, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D,
+                     "context": n_end, "realised_cr": wl.B * wl.Hkv * n_end / len_sum,
+                     "step_tokens_per_s": wl.B / (step_us * 1e-6), "step_us": step_us,
+                     "decode_us": dec_us, "decode_GBps": gbs, "decode_frac_of_measured_copy": gbs / peak})
+        del qs, ks, vs, ls
+        torch.cuda.empty_cache()
+    return rows
+
+
 def decode_bytes_fp8(wl, len_sum):
     """Algorithmic bytes of one decode call on an FP8 cache: per retained slot
     the K row (D codes + its 16-byte scale chunk) and the V row (D codes); q,
@@ -696,6 +762,7 @@ def main():
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-storage leg")
     ap.add_argument("--no-graph", action="store_true", help="skip the multi-layer CUDA-graph step leg")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload decode table")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill leg and print its figures (for profiling)")
     ap.add_argument("--prefill-chunks", type=int, default=9)
@@ -818,6 +885,8 @@ def main():
                                "(one copy), append + decode, output copied out, stream synchronized every step"}
     if not args.no_variants and world == 1:
         line["variants"] = time_variants(dms, W, device, 32)
+    if not args.no_workloads and world == 1:
+        line["workloads"] = time_workloads(dms, W, device, 64)
     if not args.no_graph and world == 1:
         line["step_graph"] = time_graph_leg(dms, W, device, 32)
     if not args.no_fp8 and world == 1:

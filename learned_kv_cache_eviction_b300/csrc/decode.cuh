@@ -93,9 +93,10 @@ struct DecodeShape {
 // Largest number of warps per CTA of any instantiation (sizes the partials).
 constexpr int kMaxWarpsPerCta = 12;
 
-// Fewest retained slots a warp is given (bounds the number of partials when
-// the cache is small).
-constexpr int kMinSlotsPerWarp = 128;
+// Fewest retained slots a warp is given (two tiles; bounds the number of
+// partials when the cache is small).  Small caches are latency-bound per warp,
+// so they are spread over as many warps as this allows.
+constexpr int kMinSlotsPerWarp = 32;
 
 struct DecodeArgs {
   const uint4* K;
