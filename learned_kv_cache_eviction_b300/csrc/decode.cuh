@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   };
 
   const int Hq = a.Hkv * G;
-  TileIter is, cs;
+  TileIter is{}, cs{};
   is.start(lenf, i0, P0, A, E);
   cs = is;
   int n_issued = 0, n_cons = 0, nq_issued = 0, nq_conv = 0;
