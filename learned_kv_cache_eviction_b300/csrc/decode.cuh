@@ -106,10 +106,17 @@ struct DecodeArgs {
   float* out;         // fp32 [B][Hq][D]
   float* part_acc;    // [entries][G][D]
   float* part_ml;     // [entries][G][2]
-  int32_t* head_cnt;  // [NH] arrival counters of split heads; zero between calls
+  int32_t* head_cnt;  // [NH * nsplit] arrival counters of split (virtual) heads; zero between calls
   int32_t* err;
   int NH, Hkv, cap;
   float qscale;  // scale * log2(e)
+  // Query heads per KV head (the q / out row stride), and how many groups of
+  // G of them each KV head is split into (1, or 2 when Gq = 2 G).  With two
+  // groups the kernel works on 2 NH virtual heads: virtual head v is KV head
+  // v mod NH with query heads [(v / NH) G, (v / NH + 1) G) of its group.  Both
+  // groups stream the same K/V rows, at about the same time, so the second
+  // read is mostly served by L2.
+  int Gq, nsplit;
   // Fused step only (decode_kernel<D, G, true>, dms_step): the new token of
   // position t is appended in the same launch.  `len` is then the base of the
   // double-buffered lengths [2][NH] (see CacheView): the kernel decodes over
@@ -371,8 +378,12 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   if constexpr (FUSED) {
     if (a.t_dev != nullptr) t_step = __ldcg(a.t_dev);
   }
-  int* pre = reinterpret_cast<int*>(smem);  // [NH + 1]; aliases the warp regions until the barrier below
-  int* sn = pre + a.NH + 1;                 // fused step: [NH] the new token's slot in each head
+  // Virtual heads (see DecodeArgs::nsplit) and the KV head / query-head group of each.
+  const int NV = a.NH * a.nsplit;
+  auto real_head = [&](int v) { return v >= a.NH ? v - a.NH : v; };
+  auto head_group = [&](int v) { return v >= a.NH ? 1 : 0; };
+  int* pre = reinterpret_cast<int*>(smem);  // [NV + 1]; aliases the warp regions until the barrier below
+  int* sn = pre + NV + 1;                   // fused step: [NH] the new token's slot in each KV head
   // Fused step: warp x of the grid appends the token to head x (and x + nwarps,
   // ...).  Its row chunk (K for lanes < CH, V for lanes CH .. 2 CH - 1) and
   // logit are loaded now, in flight during the scan.
@@ -387,7 +398,8 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   }
   // The scan reads each head's length (and, fused, the ring entry of t - w) once;
   // the fused scan also records the new token's slot in sn.
-  auto scanf = [&](int x) {
+  auto scanf = [&](int v) {
+    const int x = real_head(v);
     if constexpr (FUSED) {
       const int L = a.len[(t_step & 1) * a.NH + x];
       int fl = 0, sl = 0;
@@ -396,13 +408,13 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
         fl = a.ring_flag[e];
         sl = a.ring_slot[e];
       }
-      sn[x] = fl ? sl : (L < a.cap ? L : -1);
+      if (v < a.NH) sn[x] = fl ? sl : (L < a.cap ? L : -1);
       return (fl || L >= a.cap) ? L : L + 1;
     } else {
       return a.len[x];
     }
   };
-  scan_lengths(scanf, a.NH, pre);
+  scan_lengths(scanf, NV, pre);
   if constexpr (FUSED) {
     // Bookkeeping and row of the new token; none of it is read by this launch
     // (other halves of the double-buffered state, the slot map, and a pool row
@@ -431,7 +443,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
       }
     }
   }
-  const int64_t S = pre[a.NH];
+  const int64_t S = pre[NV];
   int64_t Pe = nwarps;
   if (S / kMinSlotsPerWarp < Pe) Pe = S / kMinSlotsPerWarp;
   if (Pe < 1) Pe = 1;
@@ -441,7 +453,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   if (active) {
     A = (wg * S) / Pe;
     E = ((wg + 1) * S) / Pe;
-    int lo = 0, hi = a.NH;  // pre[lo] <= A < pre[hi]
+    int lo = 0, hi = NV;  // pre[lo] <= A < pre[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (pre[mid] <= A) lo = mid; else hi = mid;
@@ -453,7 +465,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   // barrier, which ends the prefix sums' lease on the warp regions).
   int snl = -1;
   if constexpr (FUSED) {
-    if (active && lane < Sh::FX_HEADS && i0 + lane < a.NH) snl = sn[i0 + lane];
+    if (active && lane < Sh::FX_HEADS && i0 + lane < NV) snl = sn[real_head(i0 + lane)];
   }
   __syncthreads();
 
@@ -482,12 +494,12 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   __syncwarp();
   // Retained length of head x after this launch's append (read per head
   // change; the position comes from shared memory, not a register).
-  auto lenf = [&](int x) {
-    if constexpr (FUSED) return decode_len<true>(a, *reinterpret_cast<const int64_t*>(fx + Sh::FX_T), x);
-    else return decode_len<false>(a, 0, x);
+  auto lenf = [&](int v) {
+    if constexpr (FUSED) return decode_len<true>(a, *reinterpret_cast<const int64_t*>(fx + Sh::FX_T), real_head(v));
+    else return decode_len<false>(a, 0, real_head(v));
   };
 
-  const int Hq = a.Hkv * G;
+  const int Hq = a.Hkv * a.Gq;
   TileIter is{}, cs{};
   is.start(lenf, i0, P0, A, E);
   cs = is;
@@ -505,14 +517,16 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
       const int buf = n_issued % NST;
       if (lane == 0) {
         const uint32_t kbytes = static_cast<uint32_t>(cnt * ROWB_K), vbytes = static_cast<uint32_t>(cnt * ROWB_V);
-        const size_t row = static_cast<size_t>(is.i) * a.cap + is.s;
+        const size_t row = static_cast<size_t>(real_head(is.i)) * a.cap + is.s;
         mbar_arrive_expect_tx(&bars[buf], kbytes + vbytes);
         bulk_copy_g2s(Ks + buf * TILEB_K, a.K + row * Sh::KU4, kbytes, &bars[buf]);
         bulk_copy_g2s(Vs + buf * TILEB_V, a.V + row * Sh::VU4, vbytes, &bars[buf]);
       }
       if (is.first) {
-        const int b = is.i / a.Hkv, h = is.i - (is.i / a.Hkv) * a.Hkv;
-        const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * Hq + h * G) * D);
+        const int x = real_head(is.i);
+        const int b = x / a.Hkv, h = x - (x / a.Hkv) * a.Hkv;
+        const uint4* qsrc =
+            reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * Hq + h * a.Gq + head_group(is.i) * G) * D);
 #pragma unroll
         for (int v = 0; v < QV; ++v) {
           const int x = lane + 32 * v;
@@ -521,7 +535,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
         ++nq_issued;
       }
       ++n_issued;
-      is.advance(lenf, a.NH, cnt);
+      is.advance(lenf, NV, cnt);
     }
   };
 
@@ -572,7 +586,8 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
       if constexpr (FUSED) {
         const int d = cs.i - fx[Sh::FX_I0];
         const int sw =
-            d < Sh::FX_HEADS ? fx[d] : fused_new_slot_far(a, *reinterpret_cast<const int64_t*>(fx + Sh::FX_T), cs.i);
+            d < Sh::FX_HEADS ? fx[d]
+                             : fused_new_slot_far(a, *reinterpret_cast<const int64_t*>(fx + Sh::FX_T), real_head(cs.i));
         __syncwarp();
         if (lane == 0) fx[Sh::FX_SEG] = sw;
         __syncwarp();
@@ -592,7 +607,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
       const int sw = fx[Sh::FX_SEG];  // reloaded after the wait (the wait clobbers memory)
       if (static_cast<unsigned>(sw - s0) < static_cast<unsigned>(cnt))
         patch_new_row(a, reinterpret_cast<uint4*>(Ks + buf * TILEB_K), reinterpret_cast<uint4*>(Vs + buf * TILEB_V),
-                      seg_i, sw - s0, sw, CH, lane);
+                      real_head(seg_i), sw - s0, sw, CH, lane);
     }
 
     // ---- QK: lanes r and r + 16 score slot s0 + r over the two halves of D ----
@@ -754,15 +769,16 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
     __syncwarp();
     ++n_cons;
     const int cur_i = cs.i;
-    cs.advance(lenf, a.NH, cnt);
+    cs.advance(lenf, NV, cnt);
     const bool seg_end = !cs.valid || cs.i != cur_i;
 
     if (seg_end) {
       // ---- segment end: direct output, or a partial merged by the last arriver ----
 #pragma unroll
       for (int g = 0; g < G; ++g) l[g] = warp_sum(l[g]);
-      const int b = seg_i / a.Hkv, h = seg_i - b * a.Hkv;
-      float* outp = a.out + (static_cast<size_t>(b) * Hq + h * G) * D + lane * EL;
+      const int x = real_head(seg_i);
+      const int b = x / a.Hkv, h = x - b * a.Hkv;
+      float* outp = a.out + (static_cast<size_t>(b) * Hq + h * a.Gq + head_group(seg_i) * G) * D + lane * EL;
       // Warps holding the first and the last slot of this head.
       const int64_t w0 = ((seg_P + 1) * Pe - 1) / S;
       const int64_t w1 = ((seg_P + seg_L) * Pe - 1) / S;

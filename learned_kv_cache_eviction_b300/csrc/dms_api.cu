@@ -27,7 +27,7 @@ struct dms_cache {
   dms::CacheView view;
   float* part_acc;
   float* part_ml;
-  int32_t* head_cnt;  // [NH] arrival counters of heads split across warps (zero between calls)
+  int32_t* head_cnt;  // [2 NH] arrival counters of (virtual) heads split across warps (zero between calls)
   size_t part_entries;
   // The position in device memory, read by steps replayed from a CUDA graph
   // (dms_step_graph_*).  Valid while t_dev_synced; any call that advances t
@@ -134,20 +134,23 @@ int decode_attr(const dms_cache* c) {
   return DMS_OK;
 }
 
+// G: query heads per warp task; nsplit: groups per KV head (query heads per KV
+// head = G * nsplit), see dms::DecodeArgs.
 template <int D, int G, bool FUSED, int KVF>
-int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaStream_t st, const StepInput* in) {
+int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaStream_t st, const StepInput* in,
+                    int nsplit = 1) {
   using Sh = dms::DecodeShape<D, G, KVF>;
   if (decode_attr<D, G, FUSED, KVF>(c) != DMS_OK) return DMS_ERR_CUDA;
+  const int64_t NV = static_cast<int64_t>(c->NH) * nsplit;
   // The prologue's prefix sums (and, fused, each head's new slot) fit in shared memory.
-  if (static_cast<int64_t>((FUSED ? 2 : 1) * c->NH + 1) * 4 > Sh::SMEM) return DMS_ERR_INVALID_ARG;
+  if ((NV + 1 + (FUSED ? c->NH : 0)) * 4 > Sh::SMEM) return DMS_ERR_INVALID_ARG;
   // Upper bound of the retained slots (the exact sum lives on the device); a
   // graph-replayed step runs at positions unknown now, so it takes the capacity.
   const bool graph = FUSED && in != nullptr && in->t_dev != nullptr;
-  const int64_t smax =
-      static_cast<int64_t>(c->NH) * (graph ? c->cap : std::min<int64_t>(c->t + (FUSED ? 1 : 0), c->cap));
+  const int64_t smax = NV * (graph ? c->cap : std::min<int64_t>(c->t + (FUSED ? 1 : 0), c->cap));
   const int64_t want = (smax + int64_t(dms::kMinSlotsPerWarp) * Sh::NW - 1) / (int64_t(dms::kMinSlotsPerWarp) * Sh::NW);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(c->num_sms, want)));
-  if (static_cast<size_t>(grid) * Sh::NW + c->NH > c->part_entries) return DMS_ERR_INVALID_ARG;
+  if (static_cast<size_t>(grid) * Sh::NW + NV > c->part_entries) return DMS_ERR_INVALID_ARG;
   dms::DecodeArgs a{};
   a.K = c->view.K;
   a.V = c->view.V;
@@ -162,6 +165,8 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
   a.Hkv = c->H;
   a.cap = c->cap;
   a.qscale = scale * 1.4426950408889634f;  // log2(e): softmax evaluated as 2^(x log2 e)
+  a.Gq = G * nsplit;
+  a.nsplit = nsplit;
   a.k_new = nullptr;
   a.v_new = nullptr;
   a.logit_new = nullptr;
@@ -197,9 +202,12 @@ int launch_decode_d(dms_cache* c, const void* q, float* out, float scale, int G,
     case 3: return launch_decode_t<D, 3, FUSED, KVF>(c, q, out, scale, st, in);
     case 4: return launch_decode_t<D, 4, FUSED, KVF>(c, q, out, scale, st, in);
     case 5: return launch_decode_t<D, 5, FUSED, KVF>(c, q, out, scale, st, in);
-    case 6: return launch_decode_t<D, 6, FUSED, KVF>(c, q, out, scale, st, in);
+    // Six and eight query heads per KV head run as two groups of three / four:
+    // the 12-warp kernel of the smaller group beats the 8-warp kernel that the
+    // registers of a six- or eight-head warp allow.
+    case 6: return launch_decode_t<D, 3, FUSED, KVF>(c, q, out, scale, st, in, 2);
     case 7: return launch_decode_t<D, 7, FUSED, KVF>(c, q, out, scale, st, in);
-    case 8: return launch_decode_t<D, 8, FUSED, KVF>(c, q, out, scale, st, in);
+    case 8: return launch_decode_t<D, 4, FUSED, KVF>(c, q, out, scale, st, in, 2);
     default: return DMS_ERR_INVALID_ARG;
   }
 }
@@ -250,9 +258,9 @@ int fused_attr_d(const dms_cache* c, int G) {
     case 3: return decode_attr<D, 3, true, dms::kKvBf16>(c);
     case 4: return decode_attr<D, 4, true, dms::kKvBf16>(c);
     case 5: return decode_attr<D, 5, true, dms::kKvBf16>(c);
-    case 6: return decode_attr<D, 6, true, dms::kKvBf16>(c);
+    case 6: return decode_attr<D, 3, true, dms::kKvBf16>(c);
     case 7: return decode_attr<D, 7, true, dms::kKvBf16>(c);
-    case 8: return decode_attr<D, 8, true, dms::kKvBf16>(c);
+    case 8: return decode_attr<D, 4, true, dms::kKvBf16>(c);
     default: return DMS_ERR_INVALID_ARG;
   }
 }
@@ -392,7 +400,8 @@ dms_cache_t* dms_cache_create_ex(int batch, int kv_heads, int capacity, int head
   const size_t vpool = static_cast<size_t>(NH) * capacity * (fp8 ? head_dim : 2 * head_dim);
   const size_t nslot = static_cast<size_t>(NH) * capacity;
   const size_t nring = 2 * static_cast<size_t>(NH) * window;  // two generations
-  c->part_entries = static_cast<size_t>(c->num_sms) * dms::kMaxWarpsPerCta + NH;
+  // partials: one per warp and virtual head (two per KV head when its query heads are split)
+  c->part_entries = static_cast<size_t>(c->num_sms) * dms::kMaxWarpsPerCta + 2 * NH;
   const size_t part_acc = c->part_entries * DMS_MAX_GROUP * head_dim * sizeof(float);
   const size_t part_ml = c->part_entries * DMS_MAX_GROUP * 2 * sizeof(float);
   bool ok = cudaMalloc(&c->view.K, kpool) == cudaSuccess && cudaMalloc(&c->view.V, vpool) == cudaSuccess &&
@@ -401,12 +410,12 @@ dms_cache_t* dms_cache_create_ex(int batch, int kv_heads, int capacity, int head
             cudaMalloc(&c->view.ring_flag, nring) == cudaSuccess &&
             cudaMalloc(&c->view.len, 2 * NH * 4) == cudaSuccess && cudaMalloc(&c->view.err, kAlign) == cudaSuccess &&
             cudaMalloc(&c->part_acc, part_acc) == cudaSuccess && cudaMalloc(&c->part_ml, part_ml) == cudaSuccess &&
-            cudaMalloc(&c->head_cnt, NH * 4) == cudaSuccess;
+            cudaMalloc(&c->head_cnt, 2 * NH * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->view.K, 0, kpool) == cudaSuccess && cudaMemset(c->view.V, 0, vpool) == cudaSuccess &&
        cudaMemset(c->view.slot_pos, 0xff, nslot * 4) == cudaSuccess &&
        cudaMemset(c->view.ring_slot, 0xff, nring * 4) == cudaSuccess &&
        cudaMemset(c->view.ring_flag, 0, nring) == cudaSuccess && cudaMemset(c->view.len, 0, 2 * NH * 4) == cudaSuccess &&
-       cudaMemset(c->view.err, 0, kAlign) == cudaSuccess && cudaMemset(c->head_cnt, 0, NH * 4) == cudaSuccess &&
+       cudaMemset(c->view.err, 0, kAlign) == cudaSuccess && cudaMemset(c->head_cnt, 0, 2 * NH * 4) == cudaSuccess &&
        cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     cudaGetLastError();

@@ -126,6 +126,8 @@ int run(int dev, int num_sms, unsigned char* scratch, const void* k_pool, const 
   a.Hkv = kv_heads;
   a.cap = capacity;
   a.qscale = scale * 1.4426950408889634f;  // log2(e)
+  a.Gq = G;
+  a.nsplit = 1;
   // The merge in the decode kernel needs every head counter at zero.  Calls that
   // complete leave them at zero; clearing them here (stream-ordered, no
   // allocation) also recovers from a call that stopped early.

@@ -126,7 +126,9 @@ def test_tiny_every_step():
     ("mha-d128", 2, 3, 3, 128, 16, 300, ("normal", 0.0, 1.0), 300),
     ("g3-d64", 3, 6, 2, 64, 16, 200, ("normal", 0.5, 1.0), 200),
     ("g5-d128", 2, 10, 2, 128, 16, 260, ("normal", 1.15, 1.0), 260),
-    ("g8-d128", 1, 64, 8, 128, 16, 200, ("normal", 2.0, 1.5), 200),
+    ("g8-d128", 1, 64, 8, 128, 16, 200, ("normal", 2.0, 1.5), 200),  # two groups of 4 per KV head
+    ("g6-d64", 2, 12, 2, 64, 16, 180, ("normal", 0.8, 1.0), 180),     # two groups of 3 per KV head
+    ("g6-d128-many", 24, 48, 8, 128, 16, 90, ("normal", 0.5, 1.0), 90),
     ("g7-d64", 1, 14, 2, 64, 4, 130, ("normal", 0.3, 2.0), 130),
     ("eager-w1", 2, 8, 2, 128, 1, 150, ("normal", 0.0, 1.0), 150),
     ("short-T-below-w", 2, 8, 2, 64, 16, 16, ("normal", 1.0, 1.0), 10),
@@ -358,7 +360,8 @@ def test_device_wait_time_limit_is_reported():
     # B, Hq, Hkv, D, w, cap, T, logits
     (2, 8, 2, 128, 16, 300, 260, ("normal", 0.6, 1.0)),    # G 4: new slots inside tiles and at their edges
     (3, 3, 3, 64, 1, 200, 150, ("normal", 0.0, 1.0)),      # MHA, d64, eager eviction
-    (2, 16, 2, 128, 40, 200, 180, ("normal", 1.15, 1.0)),  # G 8, window 40
+    (2, 16, 2, 128, 40, 200, 180, ("normal", 1.15, 1.0)),  # G 8 (two groups of 4), window 40
+    (3, 18, 3, 64, 16, 150, 120, ("normal", 0.4, 1.0)),    # G 6 (two groups of 3)
     (1, 10, 2, 64, 5, 100, 130, ("const", -10.0)),         # G 5, the cache fills at t = 100 (capacity error)
     (128, 8, 8, 64, 1, 8, 40, ("const", 10.0)),            # 1024 heads of length 1: > 32 heads per warp
 ])
