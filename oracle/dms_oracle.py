@@ -19,7 +19,7 @@ Sources (web pages on the method; cited by title and section):
 * Same paper, English abstract (chatpaper page): DMS delays token eviction
   rather than discarding tokens early.
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
 
 * Decision at inference: ``e = (logit > 0)`` evaluated on the float32 logit,
   which is the threshold ``sigmoid(logit) > 0.5`` without the rounding of a

@@ -7,8 +7,8 @@ does.  It shares no code with the CUDA path.
 Source: "Inference-Time Hyper-Scaling with KV Cache Compression", paper-notes
 page, section "Related work" (KVQuant / KIVI): quantization compresses the KV
 cache along an axis orthogonal to DMS's sparsification, and the two can be
-combined.  The pages fix no quantization scheme.  The reading used here (also
-listed in the design doc) is the plainest one with native hardware support:
+combined.  The pages fix no quantization scheme.  The reading used here is
+the plainest one with native hardware support:
 
 * every retained K row and every V row (one token, one KV head, D values) is
   stored as D FP8 E4M3 codes and one float32 scale;
@@ -29,7 +29,7 @@ bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 encodes
 subnormals m * 2^-9; exponent field 15 with mantissa 7 is NaN; there is no
 infinity; the largest finite magnitude is 1.75 * 2^8 = 448.
 
-Parity status: pinned by ``tests/test_oracle_pins.py`` (fp8 section): the
+Parity status: pinned by ``tests/test_fp8_oracle_pins.py``: the
 decoding of all 256 codes against the format definition written out bit by
 bit and against PyTorch's float8_e4m3fn type, the rounding against PyTorch's
 float32 -> float8_e4m3fn conversion on random and tie inputs, the encode /

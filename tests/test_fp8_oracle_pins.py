@@ -12,8 +12,8 @@ functions and require that some check fails.
 
 Source of the storage scheme: "Inference-Time Hyper-Scaling with KV Cache
 Compression", paper-notes page, "Related work" (quantization is orthogonal to
-DMS and combinable); the scheme itself is this build's reading (per-row
-absmax scale, E4M3 codes), stated in the oracle's docstring.
+DMS and combinable); the scheme itself (per-row absmax scale, E4M3 codes) is
+a reading of that remark, stated in the oracle's docstring.
 """
 import numpy as np
 import pytest
