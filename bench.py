@@ -265,15 +265,19 @@ def time_device_leg(dms, cache, ins, warmup, steps, scale, device, clocks=None, 
     total_ms = t_start.elapsed_time(t_stop)
     len1 = int(cache.lengths().sum())
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for j in range(steps):
         i = warmup + steps + j
+        eva[j][0].record(stream)
         append(i)
+        eva[j][1].record(stream)
         ev[j][0].record(stream)
         decode(i)
         ev[j][1].record(stream)
     torch.cuda.synchronize(device)
     len2 = int(cache.lengths().sum())
     dec = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    app = [a.elapsed_time(b) * 1e3 for a, b in eva]
     last = warmup + 2 * steps - 1
     c_start = torch.cuda.Event(enable_timing=True)
     c_stop = torch.cuda.Event(enable_timing=True)
@@ -285,7 +289,7 @@ def time_device_leg(dms, cache, ins, warmup, steps, scale, device, clocks=None, 
     st = cache.status()
     if st != dms.DMS_OK:
         raise dms.DmsError(st, "device status after the timed steps")
-    return {"total_ms": total_ms, "decode_us_call": statistics.mean(dec),
+    return {"total_ms": total_ms, "decode_us_call": statistics.mean(dec), "append_us_call": statistics.mean(app),
             "decode_us_call_median": statistics.median(dec),
             "decode_us": c_start.elapsed_time(c_stop) * 1e3 / steps,
             "len_sum_start": len0, "len_sum_end": len1, "len_sum_b": 0.5 * (len1 + len2), "len_sum_c": len2}
@@ -405,19 +409,58 @@ def oracle_timer(wl, n_ctx, rows):
     return run
 
 
-def cpu_baseline(wl, n_ctx, seconds=12.0, rows=(0, 1)):
+def cpu_baseline(wl, n_ctx, seconds=12.0, rows=(0, 1), one_core_seconds=4.0):
+    """The oracle timed on the host's cores (its BLAS threads), then on one
+    core for a shorter sample."""
     run = oracle_timer(wl, n_ctx, list(rows))
-    t0 = time.perf_counter()
-    steps = 0
-    while True:
-        run(n_ctx - 1 - (steps % 256))
-        steps += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": len(rows) * steps / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+
+    def sample(limit):
+        t0 = time.perf_counter()
+        steps = 0
+        while True:
+            run(n_ctx - 1 - (steps % 256))
+            steps += 1
+            if time.perf_counter() - t0 >= limit:
+                break
+        return steps, time.perf_counter() - t0
+
+    steps, dt = sample(seconds)
+    line = {"value": len(rows) * steps / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
             "sample": f"oracle decode step (mask + dense softmax attention) for batch rows {list(rows)} of "
                       f"{wl.B} at positions {n_ctx - min(steps, 256)}..{n_ctx - 1} ({steps} steps, {dt:.1f} s)"}
+    one = one_core_sample(wl.name, n_ctx, list(rows), one_core_seconds)
+    if one is not None:
+        line["one_core"] = one
+    return line
+
+
+def one_core_sample(name, n_ctx, rows, seconds):
+    """The oracle's decode step on one core: a child process whose BLAS and
+    OpenMP pools are limited to one thread by its environment."""
+    import subprocess
+    code = (
+        "import json, sys, time\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import bench\n"
+        "from learned_kv_cache_eviction_b300 import workload as W\n"
+        f"run = bench.oracle_timer(W.WORKLOADS[{name!r}], {n_ctx}, {rows!r})\n"
+        "t0 = time.perf_counter(); n = 0\n"
+        f"while time.perf_counter() - t0 < {seconds}:\n"
+        f"    run({n_ctx} - 1 - (n % 256)); n += 1\n"
+        "dt = time.perf_counter() - t0\n"
+        f"print(json.dumps({{'value': {len(rows)} * n / dt, 'unit': 'tokens/s', 'cores': 1, "
+        "'sample': f'same, one thread, {n} steps, {dt:.1f} s'}))\n")
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[var] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    try:
+        res = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                             timeout=seconds + 240)
+        return json.loads(res.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
 
 
 def time_variants(dms, W, device, steps):
@@ -520,6 +563,60 @@ def time_workloads(dms, W, device, steps):
         del qs, ks, vs, ls
         torch.cuda.empty_cache()
     return rows
+
+
+def time_context_sweep(dms, W, device, names=("qwen3-8b", "qwen-r1-32b"), points=(1024, 2048, 4096, 8192, 16384),
+                       reps=20):
+    """Decode time of one layer at growing context: the cache is filled in
+    chunks up to each point, then `reps` dms_decode_attention calls are timed
+    one by one with events, each after a write of twice the L2 size (below
+    16K the retained K/V fits in L2).  Reported per point: the median call,
+    tokens/s, algorithmic GB/s and its fraction of the measured copy
+    bandwidth."""
+    lib = dms.load_library()
+    stream = torch.cuda.current_stream(device)
+    peak, _ = measured_hbm_peak()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.ones(2 * l2 // 4, dtype=torch.float32, device=device)
+    out_rows = []
+    for name in names:
+        wl = W.WORKLOADS[name]
+        cache = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w, device=device)
+        out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device=device)
+        t = 0
+        for n in points:
+            while t < n:
+                m = min(512, n - t)
+                k, v, lg = W.kv_range(wl, 0, t, t + m, device=device)
+                cache.append_chunk(k, v, lg)
+                t += m
+            q = W.q_range(wl, 0, n - 1, n, device=device)[:, :, 0].contiguous()
+            times = []
+            for r in range(reps + 3):
+                flush.sum()  # reads twice the L2 size: evicts the cache, leaves no dirty lines
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                rc = lib.dms_decode_attention(cache.handle, q.data_ptr(), out.data_ptr(), wl.scale, wl.Hq,
+                                              stream.cuda_stream)
+                e1.record(stream)
+                if rc:
+                    raise dms.DmsError(rc, f"dms_decode_attention ({name}, n={n})")
+                torch.cuda.synchronize(device)
+                if r >= 3:
+                    times.append(e0.elapsed_time(e1) * 1e3)
+            us = statistics.median(times)
+            len_sum = int(cache.lengths().sum())
+            gbs = decode_bytes(wl, len_sum) / (us * 1e-6) / 1e9
+            out_rows.append({"workload": name, "context": n, "realised_cr": wl.B * wl.Hkv * n / len_sum,
+                             "decode_us_median": us, "tokens_per_s": wl.B / (us * 1e-6), "decode_GBps": gbs,
+                             "frac_of_measured_copy": gbs / peak})
+        st = cache.status()
+        cache.close()
+        if st != dms.DMS_OK:
+            raise dms.DmsError(st, f"context sweep ({name})")
+    del flush
+    return {"note": f"L2 flushed (a {2 * l2 >> 20} MB read) before every call; median of {reps} calls, "
+                    "each timed alone with events (so each includes its launch gap)", "points": out_rows}
 
 
 def decode_bytes_fp8(wl, len_sum):
@@ -763,6 +860,7 @@ def main():
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-storage leg")
     ap.add_argument("--no-graph", action="store_true", help="skip the multi-layer CUDA-graph step leg")
     ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload decode table")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the context sweep (1K..16K)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill leg and print its figures (for profiling)")
     ap.add_argument("--prefill-chunks", type=int, default=9)
@@ -860,6 +958,7 @@ def main():
                              "frac": dec_bytes_c / (r["decode_us"] * 1e-6) / 1e9 / peak,
                              "us_per_call_events_mean": r["decode_us_call"],
                              "us_per_call_events_median": r["decode_us_call_median"],
+                             "append_us_per_call_events": r["append_us_call"],
                              "note": "per-call events sit between launches and add a launch gap to each call",
                              "tokens_per_s": wl.B / (r["decode_us"] * 1e-6),
                              "kv_token_reads_per_step": len_avg,
@@ -885,6 +984,8 @@ def main():
                                "(one copy), append + decode, output copied out, stream synchronized every step"}
     if not args.no_variants and world == 1:
         line["variants"] = time_variants(dms, W, device, 32)
+    if not args.no_sweep and world == 1:
+        line["context_sweep"] = time_context_sweep(dms, W, device)
     if not args.no_workloads and world == 1:
         line["workloads"] = time_workloads(dms, W, device, 64)
     if not args.no_graph and world == 1:
