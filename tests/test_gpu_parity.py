@@ -507,3 +507,39 @@ def test_step_graph_equals_dms_step_per_layer():
         dms.DmsStepGraph([got[0], got[0]], kb[:2], vb[:2], lb[:2], qb[:2], ob[:2], wl.scale)
     for c in ref + got + [f]:
         c.close()
+
+
+def test_qwen3_8b_decode_trajectory_1k_to_16k():
+    """The Qwen3-8B-like run as its workload describes it: a 1024-token chunked
+    fill, then 15360 decode steps through dms_step (one fused launch each) up
+    to 16384 tokens.  Bookkeeping (lengths) is checked against the slot
+    simulator after every step and the slot map at the end; attention against
+    the oracle every 1024th step and at the last step, on rows {0, B-1}."""
+    wl = W.WORKLOADS["qwen3-8b"]
+    rows = [0, wl.B - 1]
+    T0, T = wl.prefill, wl.cap
+    tr = Trajectory(wl, T, rows=rows)
+    while tr.t < T0:
+        tr.append_chunk(min(wl.chunk, T0 - tr.t))
+    tr.check_lengths()
+    q_all = W.q_range(wl, 0, T0, T)
+    out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    n_checked = 0
+    for t in range(T0, T):
+        k, v, lg = (tr.k[:, :, t].contiguous().cuda(), tr.v[:, :, t].contiguous().cuda(),
+                    tr.lg[:, :, t].contiguous().cuda())
+        q = q_all[:, :, t - T0].contiguous()
+        tr.cache.step(k, v, lg, q.cuda(), out, scale=wl.scale)
+        tr.sim.append(tr.e[:, :, t])
+        tr.t += 1
+        tr.check_lengths()
+        if (t + 1) % 1024 == 0 or t == T - 1:
+            ref = O.decode_attention(q[rows].float().numpy(), tr.k_np, tr.v_np, tr.e[rows], t, wl.w, wl.scale)
+            assert_attention_close(out.cpu().numpy()[rows], ref, f"qwen3-8b trajectory t={t}")
+            n_checked += 1
+    assert n_checked == 15  # t + 1 = 2048, 3072, ..., 16384
+    assert tr.cache.status() == dms.DMS_OK
+    tr.check_slots()
+    cr = T / tr.sim.len.mean()
+    assert 7.0 < cr < 9.0, cr
+    tr.cache.close()
