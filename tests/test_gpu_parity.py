@@ -439,13 +439,15 @@ def test_variant_workloads_sampled(name, T):
     _prefill_then_decode(wl, T, 4, rows=[0, wl.B - 1])
 
 
-def test_step_graph_equals_dms_step_per_layer():
+@pytest.mark.parametrize("shape", [(2, 8, 2, 128), (2, 16, 2, 64)])  # G 4; G 8 (two groups of 4), d64
+def test_step_graph_equals_dms_step_per_layer(shape):
     """A 3-layer decode step captured into a CUDA graph and replayed per token
     gives the same outputs and cache state, bit for bit, as dms_step on each
     layer's cache.  Between replays one layer also advances outside the graph
     (dms_append + dms_decode_attention on both sides), which the next replay
     must pick up from the host's position."""
-    wl = _small("graph", 2, 8, 2, 128, 16, 300, ("normal", 0.6, 1.0), seed=17)
+    B, Hq, Hkv, D = shape
+    wl = _small("graph", B, Hq, Hkv, D, 16, 300, ("normal", 0.6, 1.0), seed=17)
     L, T0, T = 3, 40, 120
     data = [tuple(x.cuda() for x in W.kv_range(wl, layer, 0, T)) + (W.q_range(wl, layer, 0, T).cuda(),)
             for layer in range(L)]
