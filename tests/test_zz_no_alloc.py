@@ -38,7 +38,8 @@ def _close(got: torch.Tensor, ref: torch.Tensor):
     return float(d.max()), float(d.sum() / ref.double().abs().sum())
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,D,cap,T", [(4, 32, 8, 128, 700, 600), (2, 4, 2, 64, 300, 280)])
+@pytest.mark.parametrize("B,Hq,Hkv,D,cap,T", [(4, 32, 8, 128, 700, 600), (2, 4, 2, 64, 300, 280),
+                                            (2, 16, 2, 128, 400, 350)])  # G 8: one eight-head group here
 def test_noalloc_matches_decode_attention_twice(B, Hq, Hkv, D, cap, T):
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
