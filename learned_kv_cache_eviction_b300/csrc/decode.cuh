@@ -42,8 +42,11 @@ struct DecodeShape {
   static constexpr int G = G_;
   static constexpr int KVF = KVF_;
   static constexpr bool FP8 = KVF == kKvFp8;
-  static constexpr int TK = 16;                 // slots per tile
-  static constexpr int NST = FP8 ? 3 : 2;       // tiles in flight per warp
+  // Slots per tile: 16 (bf16; lanes r and r + 16 score slot r over the two
+  // halves of D), or 32 (fp8; the same two lanes score slots r and r + 16, so
+  // each q load serves two slots).
+  static constexpr int TK = FP8 ? 32 : 16;
+  static constexpr int NST = 2;                 // tiles in flight per warp
   static constexpr int CH = D / 8;              // 16-byte chunks per bf16 row
   static constexpr int HCH = CH / 2;            // chunks per half row (two lanes score one slot)
   static constexpr int EL = D / 32;             // output elements per lane in PV
@@ -610,69 +613,29 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
                       real_head(seg_i), sw - s0, sw, CH, lane);
     }
 
-    // ---- QK: lanes r and r + 16 score slot s0 + r over the two halves of D ----
-    float sc[G];
-    float vsc = 0.f;  // fp8: the slot's V scale (folded into its probability)
+    // ---- QK and online softmax (base 2) ----
     if constexpr (!Sh::FP8) {
-      const uint4* krow = reinterpret_cast<const uint4*>(Ks + buf * TILEB_K) + r * CH;
-      const int sw = (s0 + r) & 7;
-      const float* qh = qs + hf * QHALF;
-      float2 acc0[G], acc1[G];
+      // QK: lanes r and r + 16 score slot s0 + r over the two halves of D
+      float sc[G];
+      {
+        const uint4* krow = reinterpret_cast<const uint4*>(Ks + buf * TILEB_K) + r * CH;
+        const int sw = (s0 + r) & 7;
+        const float* qh = qs + hf * QHALF;
+        float2 acc0[G], acc1[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        acc0[g] = make_float2(0.f, 0.f);
-        acc1[g] = make_float2(0.f, 0.f);
-      }
-      if (r < cnt) {
-#pragma unroll
-        for (int c = 0; c < HCH; ++c) {
-          const uint4 kk = krow[(hf * HCH + c) ^ sw];
-          const float2 k0 = bf16x2_to_float2(kk.x), k1 = bf16x2_to_float2(kk.y);
-          const float2 k2 = bf16x2_to_float2(kk.z), k3 = bf16x2_to_float2(kk.w);
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float4* qp = reinterpret_cast<const float4*>(qh + g * QROW + c * 8);
-            const float4 qa = qp[0], qb = qp[1];
-            acc0[g] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc0[g]);
-            acc1[g] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc1[g]);
-            acc0[g] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc0[g]);
-            acc1[g] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc1[g]);
-          }
+        for (int g = 0; g < G; ++g) {
+          acc0[g] = make_float2(0.f, 0.f);
+          acc1[g] = make_float2(0.f, 0.f);
         }
-      }
+        if (r < cnt) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float sg = (acc0[g].x + acc0[g].y) + (acc1[g].x + acc1[g].y);
-        sg += __shfl_xor_sync(0xffffffffu, sg, 16);
-        sc[g] = r < cnt ? sg : -INFINITY;
-      }
-    } else {
-      // fp8: the lane's half row is D / 32 units of 16 codes; the score is the
-      // dot product with the codes times the row's K scale.
-      const uint8_t* krow = Ks + buf * TILEB_K + r * ROWB_K;
-      const float* qh = qs + hf * QHALF;
-      float2 acc0[G], acc1[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        acc0[g] = make_float2(0.f, 0.f);
-        acc1[g] = make_float2(0.f, 0.f);
-      }
-      float ksc = 0.f;
-      if (r < cnt) {
-        const float2 kv = *reinterpret_cast<const float2*>(krow + D);
-        ksc = kv.x;
-        vsc = kv.y;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          const uint4 kk = *reinterpret_cast<const uint4*>(krow + hf * (D / 2) + c * 16);
-#pragma unroll
-          for (int hw = 0; hw < 2; ++hw) {  // 8 codes at a time
-            const uint32_t w0 = hw ? kk.z : kk.x, w1 = hw ? kk.w : kk.y;
-            const float2 k0 = e4m3x2_to_float2(w0 & 0xffffu), k1 = e4m3x2_to_float2(w0 >> 16);
-            const float2 k2 = e4m3x2_to_float2(w1 & 0xffffu), k3 = e4m3x2_to_float2(w1 >> 16);
+          for (int c = 0; c < HCH; ++c) {
+            const uint4 kk = krow[(hf * HCH + c) ^ sw];
+            const float2 k0 = bf16x2_to_float2(kk.x), k1 = bf16x2_to_float2(kk.y);
+            const float2 k2 = bf16x2_to_float2(kk.z), k3 = bf16x2_to_float2(kk.w);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-              const float4* qp = reinterpret_cast<const float4*>(qh + g * QROW + c * 16 + hw * 8);
+              const float4* qp = reinterpret_cast<const float4*>(qh + g * QROW + c * 8);
               const float4 qa = qp[0], qb = qp[1];
               acc0[g] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc0[g]);
               acc1[g] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc1[g]);
@@ -681,37 +644,128 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
             }
           }
         }
-      }
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float sg = (acc0[g].x + acc0[g].y) + (acc1[g].x + acc1[g].y);
-        sg += __shfl_xor_sync(0xffffffffu, sg, 16);
-        sc[g] = r < cnt ? sg * ksc : -INFINITY;
+        for (int g = 0; g < G; ++g) {
+          float sg = (acc0[g].x + acc0[g].y) + (acc1[g].x + acc1[g].y);
+          sg += __shfl_xor_sync(0xffffffffu, sg, 16);
+          sc[g] = r < cnt ? sg : -INFINITY;
+        }
       }
-    }
 
-    // ---- online softmax (base 2); lanes r and r + 16 hold the same scores ----
-    {
-      bool rescale = false;
-      float alpha[G], p[G];
+      // ---- online softmax (base 2); lanes r and r + 16 hold the same scores ----
+      {
+        bool rescale = false;
+        float alpha[G], p[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float mt = sc[g];
+#pragma unroll
+          for (int off = 8; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+          const float mn = fmaxf(m[g], mt);
+          alpha[g] = fast_exp2(m[g] - mn);
+          p[g] = fast_exp2(sc[g] - mn);
+          l[g] = l[g] * alpha[g] + (hf == 0 ? p[g] : 0.f);
+          m[g] = mn;
+          rescale |= alpha[g] != 1.f;
+        }
+        if (hf == 0) {
+          float2* prow = reinterpret_cast<float2*>(pb + r * PROW);
+#pragma unroll
+          for (int g = 0; g < G; ++g) prow[g] = make_float2(p[g], p[g]);
+        }
+        if (rescale) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float2 aa = make_float2(alpha[g], alpha[g]);
+#pragma unroll
+            for (int e = 0; e < EL / 2; ++e) o[g][e] = __fmul2_rn(o[g][e], aa);
+          }
+        }
+        __syncwarp();
+      }
+    } else {
+      // fp8, 32-slot tiles: lanes r and r + 16 score slots s0 + r and s0 + r + 16
+      // over the two halves of D, each q load serving both slots.  A score is
+      // the dot product with the codes times the row's K scale; the V scale is
+      // folded into the slot's probability for PV.  Rows at or past cnt hold
+      // stale bytes: their scores are replaced by -inf and their V scales by 0.
+      const uint8_t* krA = Ks + buf * TILEB_K + r * ROWB_K;
+      const uint8_t* krB = krA + 16 * ROWB_K;
+      const bool okA = r < cnt, okB = r + 16 < cnt;
+      const float* qh = qs + hf * QHALF;
+      float2 aA0[G], aA1[G], aB0[G], aB1[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float mt = sc[g];
+        aA0[g] = make_float2(0.f, 0.f);
+        aA1[g] = make_float2(0.f, 0.f);
+        aB0[g] = make_float2(0.f, 0.f);
+        aB1[g] = make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        const uint4 kA = *reinterpret_cast<const uint4*>(krA + hf * (D / 2) + c * 16);
+        const uint4 kB = *reinterpret_cast<const uint4*>(krB + hf * (D / 2) + c * 16);
+#pragma unroll
+        for (int hw = 0; hw < 2; ++hw) {  // 8 codes of each slot at a time
+          const uint32_t wa0 = hw ? kA.z : kA.x, wa1 = hw ? kA.w : kA.y;
+          const uint32_t wb0 = hw ? kB.z : kB.x, wb1 = hw ? kB.w : kB.y;
+          const float2 a0 = e4m3x2_to_float2(wa0 & 0xffffu), a1 = e4m3x2_to_float2(wa0 >> 16);
+          const float2 a2 = e4m3x2_to_float2(wa1 & 0xffffu), a3 = e4m3x2_to_float2(wa1 >> 16);
+          const float2 b0 = e4m3x2_to_float2(wb0 & 0xffffu), b1 = e4m3x2_to_float2(wb0 >> 16);
+          const float2 b2 = e4m3x2_to_float2(wb1 & 0xffffu), b3 = e4m3x2_to_float2(wb1 >> 16);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float4* qp = reinterpret_cast<const float4*>(qh + g * QROW + c * 16 + hw * 8);
+            const float4 qa = qp[0], qb = qp[1];
+            const float2 q01 = make_float2(qa.x, qa.y), q23 = make_float2(qa.z, qa.w);
+            const float2 q45 = make_float2(qb.x, qb.y), q67 = make_float2(qb.z, qb.w);
+            aA0[g] = __ffma2_rn(q01, a0, aA0[g]);
+            aA1[g] = __ffma2_rn(q23, a1, aA1[g]);
+            aA0[g] = __ffma2_rn(q45, a2, aA0[g]);
+            aA1[g] = __ffma2_rn(q67, a3, aA1[g]);
+            aB0[g] = __ffma2_rn(q01, b0, aB0[g]);
+            aB1[g] = __ffma2_rn(q23, b1, aB1[g]);
+            aB0[g] = __ffma2_rn(q45, b2, aB0[g]);
+            aB1[g] = __ffma2_rn(q67, b3, aB1[g]);
+          }
+        }
+      }
+      const float2 scA = *reinterpret_cast<const float2*>(krA + D);  // {K scale, V scale}
+      const float2 scB = *reinterpret_cast<const float2*>(krB + D);
+      const float vsA = okA ? scA.y : 0.f, vsB = okB ? scB.y : 0.f;
+      float sA[G], sB[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float x = (aA0[g].x + aA0[g].y) + (aA1[g].x + aA1[g].y);
+        float y = (aB0[g].x + aB0[g].y) + (aB1[g].x + aB1[g].y);
+        x += __shfl_xor_sync(0xffffffffu, x, 16);
+        y += __shfl_xor_sync(0xffffffffu, y, 16);
+        sA[g] = okA ? x * scA.x : -INFINITY;
+        sB[g] = okB ? y * scB.x : -INFINITY;
+      }
+      // online softmax over the 32 slots; lanes r and r + 16 hold the same scores
+      bool rescale = false;
+      float alpha[G], pA[G], pB[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float mt = fmaxf(sA[g], sB[g]);
 #pragma unroll
         for (int off = 8; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
         const float mn = fmaxf(m[g], mt);
         alpha[g] = fast_exp2(m[g] - mn);
-        p[g] = fast_exp2(sc[g] - mn);
-        l[g] = l[g] * alpha[g] + (hf == 0 ? p[g] : 0.f);
+        pA[g] = fast_exp2(sA[g] - mn);
+        pB[g] = fast_exp2(sB[g] - mn);
+        l[g] = l[g] * alpha[g] + (hf == 0 ? pA[g] + pB[g] : 0.f);
         m[g] = mn;
         rescale |= alpha[g] != 1.f;
       }
-      if (hf == 0) {
-        // fp8: the weight of the slot's V codes is its probability times its V scale
-        float2* prow = reinterpret_cast<float2*>(pb + r * PROW);
+      {
+        // lane r writes slot r's weights, lane r + 16 slot r + 16's
+        float2* prow = reinterpret_cast<float2*>(pb + (r + hf * 16) * PROW);
+        const float vs = hf ? vsB : vsA;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float pw = Sh::FP8 ? p[g] * vsc : p[g];
+          const float pw = (hf ? pB[g] : pA[g]) * vs;
           prow[g] = make_float2(pw, pw);
         }
       }
