@@ -82,9 +82,11 @@ dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_di
  * (scores and probabilities are computed in fp32 as for bf16 storage).  Pools:
  * K rows of head_dim + 16 bytes (codes, then {K scale, V scale} and 8 bytes of
  * padding), V rows of head_dim bytes, i.e. 2 * head_dim + 16 bytes per slot
- * against 4 * head_dim for bf16.  On an FP8 cache dms_prefill returns
- * DMS_ERR_INVALID_ARG (its tensor-core kernel reads bf16 rows), and dms_step
- * runs as two launches (append, then decode).  dms_decode_attention_noalloc
+ * against 4 * head_dim for bf16.  On an FP8 cache dms_prefill runs its
+ * definition, `chunk` rounds of append + decode (one decode launch per token,
+ * exact, far slower than the tensor-core path of bf16 caches), and dms_step
+ * runs as two launches (append, then decode).  An FP8 cache also holds a
+ * buffer for one token's rows of those rounds.  dms_decode_attention_noalloc
  * reads bf16 pools only.
  */
 dms_cache_t* dms_cache_create_ex(int batch, int kv_heads, int capacity, int head_dim, int window, int kv_format);
@@ -138,7 +140,9 @@ int dms_append_chunk(dms_cache_t* cache, const void* k, const void* v, const flo
  * for eviction stays visible for the w - 1 positions after its own.  The
  * attention runs on the tensor cores (bf16 Q K^T, fp32 softmax, P V with p
  * carried as two bf16 terms, fp32 accumulation); then the chunk is appended
- * as by dms_append_chunk.  q_heads as for dms_decode_attention.
+ * as by dms_append_chunk.  q_heads as for dms_decode_attention.  On an FP8
+ * cache (dms_cache_create_ex) it runs the `chunk` rounds of dms_append +
+ * dms_decode_attention themselves, token by token.
  */
 int dms_prefill(dms_cache_t* cache, const void* q, const void* k, const void* v, const float* logits, int chunk,
                 float* out, float scale, int q_heads, void* stream);

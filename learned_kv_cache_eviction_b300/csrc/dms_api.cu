@@ -34,6 +34,9 @@ struct dms_cache {
   // outside a graph clears the flag, and the next graph launch re-sends t.
   int64_t* t_dev;
   bool t_dev_synced;
+  // FP8 caches: one token's rows for the prefill's rounds of append + decode
+  // (q bf16 [B][8 H][D] | out fp32 [B][8 H][D] | k, v bf16 [NH][D] | logit fp32 [NH]).
+  uint8_t* round_buf;
 };
 
 namespace {
@@ -334,6 +337,63 @@ void free_cache_memory(dms_cache* c) {
   cudaFree(c->part_acc);
   cudaFree(c->part_ml);
   cudaFree(c->head_cnt);
+  cudaFree(c->round_buf);
+}
+
+// Byte offsets into dms_cache::round_buf.
+struct RoundLayout {
+  size_t q, out, k, v, logit, total;
+  explicit RoundLayout(const dms_cache* c) {
+    const size_t rows_q = static_cast<size_t>(c->NH) * DMS_MAX_GROUP, d = static_cast<size_t>(c->D);
+    q = 0;
+    out = q + rows_q * d * 2;
+    k = out + rows_q * d * 4;
+    v = k + static_cast<size_t>(c->NH) * d * 2;
+    logit = v + static_cast<size_t>(c->NH) * d * 2;
+    total = logit + ((static_cast<size_t>(c->NH) * 4 + 255) / 256) * 256;
+  }
+};
+
+// FP8 caches: the chunked prefill as its definition states it, C rounds of
+// (append token c, decode token c's query), on the FP8 append and decode
+// kernels.  Token c's rows are gathered from the chunk layouts into the
+// cache's round buffer with pitched copies, and its output row is scattered
+// back.  Exact by construction; one decode launch per token.
+int prefill_by_rounds(dms_cache* c, const void* q, const void* k, const void* v, const float* logits, int chunk,
+                      float* out, float scale, int q_heads, cudaStream_t st) {
+  const RoundLayout lay(c);
+  uint8_t* rb = c->round_buf;
+  const size_t D = static_cast<size_t>(c->D), C = static_cast<size_t>(chunk);
+  const size_t rows_q = static_cast<size_t>(c->B) * q_heads, rows_kv = static_cast<size_t>(c->NH);
+  const int G = q_heads / c->H;
+  for (size_t t = 0; t < C; ++t) {
+    const bool ok =
+        cudaMemcpy2DAsync(rb + lay.q, D * 2, static_cast<const uint8_t*>(q) + t * D * 2, C * D * 2, D * 2, rows_q,
+                          cudaMemcpyDeviceToDevice, st) == cudaSuccess &&
+        cudaMemcpy2DAsync(rb + lay.k, D * 2, static_cast<const uint8_t*>(k) + t * D * 2, C * D * 2, D * 2, rows_kv,
+                          cudaMemcpyDeviceToDevice, st) == cudaSuccess &&
+        cudaMemcpy2DAsync(rb + lay.v, D * 2, static_cast<const uint8_t*>(v) + t * D * 2, C * D * 2, D * 2, rows_kv,
+                          cudaMemcpyDeviceToDevice, st) == cudaSuccess &&
+        cudaMemcpy2DAsync(rb + lay.logit, 4, logits + t, C * 4, 4, rows_kv, cudaMemcpyDeviceToDevice, st) ==
+            cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      return DMS_ERR_CUDA;
+    }
+    int rc = launch_append(c, rb + lay.k, rb + lay.v, reinterpret_cast<const float*>(rb + lay.logit), st);
+    if (rc != DMS_OK) return rc;
+    c->t += 1;
+    float* o = reinterpret_cast<float*>(rb + lay.out);
+    rc = c->D == 128 ? launch_decode_f<128, false>(c, rb + lay.q, o, scale, G, st)
+                     : launch_decode_f<64, false>(c, rb + lay.q, o, scale, G, st);
+    if (rc != DMS_OK) return rc;
+    if (cudaMemcpy2DAsync(out + t * D, C * D * 4, o, D * 4, D * 4, rows_q, cudaMemcpyDeviceToDevice, st) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return DMS_ERR_CUDA;
+    }
+  }
+  return DMS_OK;
 }
 
 }  // namespace
@@ -410,7 +470,8 @@ dms_cache_t* dms_cache_create_ex(int batch, int kv_heads, int capacity, int head
             cudaMalloc(&c->view.ring_flag, nring) == cudaSuccess &&
             cudaMalloc(&c->view.len, 2 * NH * 4) == cudaSuccess && cudaMalloc(&c->view.err, kAlign) == cudaSuccess &&
             cudaMalloc(&c->part_acc, part_acc) == cudaSuccess && cudaMalloc(&c->part_ml, part_ml) == cudaSuccess &&
-            cudaMalloc(&c->head_cnt, 2 * NH * 4) == cudaSuccess;
+            cudaMalloc(&c->head_cnt, 2 * NH * 4) == cudaSuccess &&
+            (!fp8 || cudaMalloc(&c->round_buf, RoundLayout(c).total) == cudaSuccess);
   ok = ok && cudaMemset(c->view.K, 0, kpool) == cudaSuccess && cudaMemset(c->view.V, 0, vpool) == cudaSuccess &&
        cudaMemset(c->view.slot_pos, 0xff, nslot * 4) == cudaSuccess &&
        cudaMemset(c->view.ring_slot, 0xff, nring * 4) == cudaSuccess &&
@@ -485,8 +546,7 @@ int dms_prefill(dms_cache_t* c, const void* q, const void* k, const void* v, con
   if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
   if (chunk < 1 || !q || !k || !v || !logits || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
       !aligned16(logits) || !aligned16(out) || q_heads < 1 || q_heads % c->H != 0 ||
-      q_heads / c->H > DMS_MAX_GROUP || !std::isfinite(scale) || c->t + chunk > INT32_MAX ||
-      c->kvf != DMS_KV_BF16)
+      q_heads / c->H > DMS_MAX_GROUP || !std::isfinite(scale) || c->t + chunk > INT32_MAX)
     return DMS_ERR_INVALID_ARG;
   DeviceGuard g(c->device);
   if (!g.ok) return DMS_ERR_CUDA;
@@ -494,6 +554,12 @@ int dms_prefill(dms_cache_t* c, const void* q, const void* k, const void* v, con
       !device_pointer_ok(logits, c->device) || !device_pointer_ok(out, c->device))
     return DMS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c->kvf == DMS_KV_FP8_E4M3) {
+    // the tensor-core kernel reads bf16 rows; FP8 caches run the definition
+    const int rc = prefill_by_rounds(c, q, k, v, logits, chunk, out, scale, q_heads, st);
+    c->t_dev_synced = false;
+    return rc;
+  }
   dms::PrefillArgs a;
   a.K = c->view.K;
   a.V = c->view.V;

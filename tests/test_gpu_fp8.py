@@ -171,24 +171,59 @@ def test_fp8_capacity_overflow_is_reported():
     run.check_state()
 
 
-def test_fp8_calls_that_need_bf16_storage_are_refused():
+def test_fp8_format_queries_and_scale_export_refused_on_bf16():
     c = dms.DmsCache(1, 2, 64, 64, 16, kv_format="fp8")
     lib = dms.load_library()
     assert lib.dms_cache_kv_format(c.handle) == dms.DMS_KV_FP8_E4M3
-    q = torch.zeros(1, 4, 8, 64, dtype=torch.bfloat16, device="cuda")
-    k = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16, device="cuda")
-    lg = torch.zeros(1, 2, 8, dtype=torch.float32, device="cuda")
-    out = torch.empty(1, 4, 8, 64, dtype=torch.float32, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
-    assert lib.dms_prefill(c.handle, q.data_ptr(), k.data_ptr(), k.data_ptr(), lg.data_ptr(), 8, out.data_ptr(), 0.1,
-                           4, s) == dms.DMS_ERR_INVALID_ARG
-    assert c.position == 0
     b = dms.DmsCache(1, 2, 64, 64, 16)
     ks = torch.empty(1, 2, 64, dtype=torch.float32, device="cuda")
     assert lib.dms_cache_export_scales(b.handle, ks.data_ptr(), ks.data_ptr(), s) == dms.DMS_ERR_INVALID_ARG
     assert lib.dms_cache_kv_format(b.handle) == dms.DMS_KV_BF16
     c.close()
     b.close()
+
+
+@pytest.mark.parametrize("case", [
+    # B, Hq, Hkv, D, w, history T0, chunk C, logits
+    (2, 8, 2, 128, 16, 150, 70, ("normal", 0.5, 1.0)),   # G 4
+    (2, 16, 2, 64, 4, 40, 33, ("normal", 0.0, 1.0)),     # G 8 (two groups of 4), window 4
+    (1, 3, 3, 64, 16, 0, 20, ("const", -10.0)),          # MHA, empty cache, all keep
+])
+def test_fp8_prefill_equals_rounds_and_matches_oracle(case):
+    """dms_prefill on an FP8 cache runs its definition, C rounds of append +
+    decode: outputs and state equal those rounds done through the API, bit for
+    bit, and the outputs match the oracle on dequantized rows."""
+    B, Hq, Hkv, D, w, T0, C, logits = case
+    wl = _wl(B, Hq, Hkv, D, w, T0 + C + 4, logits, seed=9)
+    T = T0 + C
+    run = Fp8Run(wl, T)
+    twin = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w, kv_format="fp8")
+    if T0:
+        run.append_chunk(T0)
+        twin.append_chunk(run.k[:, :, :T0].contiguous().cuda(), run.v[:, :, :T0].contiguous().cuda(),
+                          run.lg[:, :, :T0].contiguous().cuda())
+    q = W.q_range(wl, 0, T0, T)
+    out = run.cache.prefill(q.cuda(), run.k[:, :, T0:].contiguous().cuda(), run.v[:, :, T0:].contiguous().cuda(),
+                            run.lg[:, :, T0:].contiguous().cuda(), scale=wl.scale)
+    run.sim.append_chunk(run.e[:, :, T0:T])
+    run.t = T
+    assert run.cache.position == T
+    for j in range(C):
+        t = T0 + j
+        twin.append(run.k[:, :, t].contiguous().cuda(), run.v[:, :, t].contiguous().cuda(),
+                    run.lg[:, :, t].contiguous().cuda())
+        ref = twin.decode_attention(q[:, :, j].contiguous().cuda(), scale=wl.scale)
+        assert torch.equal(out[:, :, j], ref), j
+        if j % 7 == 0 or j == C - 1:
+            oref = O.decode_attention(q[:, :, j].float().numpy(), run.k_deq, run.v_deq, run.e, t, wl.w, wl.scale)
+            _close(out[:, :, j].cpu().numpy(), oref, f"fp8 prefill {case} t={t}")
+    run.check_state()
+    for x, y in zip(run.cache.export_kv() + run.cache.export_scales(), twin.export_kv() + twin.export_scales()):
+        assert torch.equal(x, y)
+    assert run.cache.status() == twin.status() == dms.DMS_OK
+    run.cache.close()
+    twin.close()
 
 
 def test_fp8_qwen3_8b_full_size_sampled():
