@@ -159,6 +159,74 @@ def check_kv_token_reads_closed_forms():
     assert O.kv_token_reads(evict, n, w) == 3 * sum(min(t, w) for t in range(1, n + 1))
 
 
+
+# ---------------------------------------------------------------------------
+# chunked prefill: C queries at positions t0 .. t0 + C - 1 of one call
+# ---------------------------------------------------------------------------
+
+_PF_T0, _PF_C = 13, 20  # rows 13 .. 32 of a 40-token problem
+
+
+def _prefill_rows(q, k, v, e, t0, C, w, scale, prefill=None):
+    prefill = prefill or O.prefill_attention
+    return prefill(q[:, :, t0:t0 + C], k, v, e, t0, w, scale)
+
+
+def check_prefill_all_keep_is_causal(prefill=None):
+    """Every decision 'keep': the chunk's rows equal rows t0 .. t0 + C - 1 of
+    causal attention over the whole sequence (library SDPA, float64)."""
+    q, k, v = _problem(seed=21)
+    B, Hkv, T = k.shape[0], k.shape[1], k.shape[2]
+    e = O.eviction_decisions(-np.abs(_rand((B, Hkv, T), 22)) - 0.5)
+    scale = 0.41
+    t0, C = _PF_T0, _PF_C
+    got = _prefill_rows(q, k, v, e, t0, C, 16, scale, prefill)
+    ref = _sdpa(q, k, v, np.tril(np.ones((T, T), dtype=bool)), scale)[:, :, t0:t0 + C]
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def check_prefill_all_evict_is_band(prefill=None):
+    """Every decision 'evict': the chunk's rows equal those rows of attention
+    restricted to the last w keys (the band t - w + 1 .. t)."""
+    q, k, v = _problem(seed=23)
+    B, Hkv, T = k.shape[0], k.shape[1], k.shape[2]
+    e = O.eviction_decisions(np.abs(_rand((B, Hkv, T), 24)) + 0.5)
+    scale = 0.29
+    t0, C = _PF_T0, _PF_C
+    ones = torch.ones(T, T, dtype=torch.bool)
+    for w in (1, 4, 16):
+        got = _prefill_rows(q, k, v, e, t0, C, w, scale, prefill)
+        band = (torch.tril(ones) & ~torch.tril(ones, diagonal=-w)).numpy()
+        ref = _sdpa(q, k, v, band, scale)[:, :, t0:t0 + C]
+        np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def check_prefill_matches_queue(prefill=None):
+    """Random decisions: row c of the chunk attends exactly to the tokens the
+    brute-force queue holds after step t0 + c (a token marked for eviction
+    leaves w steps after it entered).  The reference is SDPA with a per-head
+    mask built from the queue, not from the oracle's visibility rule."""
+    q, k, v = _problem(seed=25)
+    B, Hq, T = q.shape[0], q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    rng = np.random.default_rng(26)
+    e = rng.random((B, Hkv, T)) < 0.6
+    scale = 0.33
+    t0, C = _PF_T0, _PF_C
+    for w in (1, 3, 5):
+        mask = np.zeros((B, Hq, C, T), dtype=bool)
+        for b in range(B):
+            for h in range(Hkv):
+                sets = _queue_visible(e[b, h], w)
+                for c in range(C):
+                    mask[b, h * G:(h + 1) * G, c, sorted(sets[t0 + c])] = True
+        got = _prefill_rows(q, k, v, e, t0, C, w, scale, prefill)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[:, :, t0:t0 + C]).double(), torch.from_numpy(k).double(),
+            torch.from_numpy(v).double(), attn_mask=torch.from_numpy(mask), scale=scale, enable_gqa=True).numpy()
+        np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
 # ---------------------------------------------------------------------------
 # pins on the real oracle
 # ---------------------------------------------------------------------------
@@ -246,6 +314,18 @@ def test_chunk_append_matches_single_appends():
         b.append(e[:, :, t])
     assert np.array_equal(a.slot_pos, b.slot_pos) and np.array_equal(a.len, b.len)
 
+
+
+def test_prefill_all_keep_equals_causal_rows():
+    check_prefill_all_keep_is_causal()
+
+
+def test_prefill_all_evict_equals_band_rows():
+    check_prefill_all_evict_is_band()
+
+
+def test_prefill_rows_match_bruteforce_queue():
+    check_prefill_matches_queue()
 
 # ---------------------------------------------------------------------------
 # planted mistakes: each one must be caught by at least one check
@@ -345,3 +425,25 @@ def test_golden_worked_examples():
             assert sorted(qsets[t]) == want_vis
             assert O.retained_length(e, t + 1, w) == ret == len(want_vis)
             assert sim.occupied_positions(0, 0).tolist() == [int(x) for x in slots.split(",")]
+
+
+def test_planted_prefill_position_and_chunk_index_slips():
+    """A query row evaluated one position early, a query taken from the wrong
+    row of the chunk, and every row evaluated at t0 are each caught."""
+    def early(q_chunk, k_hist, v_hist, e_hist, t0, w, scale):
+        C = q_chunk.shape[2]
+        return np.stack([O.decode_attention(q_chunk[:, :, c], k_hist, v_hist, e_hist, t0 + c - 1, w, scale)
+                         for c in range(C)], axis=2)
+
+    def wrong_row(q_chunk, k_hist, v_hist, e_hist, t0, w, scale):
+        C = q_chunk.shape[2]
+        return np.stack([O.decode_attention(q_chunk[:, :, (c + 1) % C], k_hist, v_hist, e_hist, t0 + c, w, scale)
+                         for c in range(C)], axis=2)
+
+    def frozen(q_chunk, k_hist, v_hist, e_hist, t0, w, scale):
+        C = q_chunk.shape[2]
+        return np.stack([O.decode_attention(q_chunk[:, :, c], k_hist, v_hist, e_hist, t0, w, scale)
+                         for c in range(C)], axis=2)
+    for bad in (early, wrong_row, frozen):
+        assert _fails(check_prefill_all_keep_is_causal, prefill=bad)
+        assert _fails(check_prefill_matches_queue, prefill=bad)
