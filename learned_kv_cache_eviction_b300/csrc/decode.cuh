@@ -79,8 +79,21 @@ struct DecodeShape {
   static constexpr int FX_I0 = FX_HEADS, FX_SEG = FX_HEADS + 1;
   static constexpr int FX_T = FX_HEADS + 2;  // the step's position t (int64, two slots)
   static constexpr int OFF_FX = OFF_BAR + NST * 8;
-  static constexpr int FX_BYTES = FP8 ? 0 : (FX_HEADS + 2) * 4;  // the fused step is bf16 only
-  static constexpr int WARP_BYTES = ((OFF_FX + FX_BYTES + 127) / 128) * 128;
+  static constexpr int FX_BYTES = FP8 ? 0 : (FX_T + 2) * 4;  // through the int64 position; bf16 only
+  // Then an mbarrier for the bulk copies of a merge, the deferred arrival of
+  // the warp's first segment (see decode_kernel): {virtual head, index of its
+  // first partial, partial count, arrivals before this warp's}, and the merge
+  // mbarrier's phase.
+  static constexpr int OFF_MB = OFF_FX + FX_BYTES;
+  static constexpr int OFF_DEF = OFF_MB + 8;
+  static constexpr int WARP_BYTES = ((OFF_DEF + 20 + 127) / 128) * 128;
+  // Partials: acc [G][D] floats, and (max, sum) of the G heads padded to a
+  // 16-byte record of MLS floats, so that consecutive partials form one
+  // contiguous bulk copy.  A merge stages up to PM of them at a time in the
+  // warp's tile buffers, which are free once its range is done.
+  static constexpr int MLS = (2 * G + 3) / 4 * 4;
+  static constexpr int STAGE_BYTES = NST * (TILEB_K + TILEB_V);
+  static constexpr int PM = STAGE_BYTES / (G * D * 4 + MLS * 4);
   static constexpr int kSmemBudget = 227 * 1024 - 1024;  // leaves room for static shared memory
   // Warps per CTA: 12 (three per scheduler) where the shared memory allows.  With
   // three warps on a scheduler its register file leaves 168 registers per thread;
@@ -91,14 +104,18 @@ struct DecodeShape {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(G >= 1 && G <= 8, "1 <= G <= 8");
   static_assert(NW >= 4, "at least four warps per CTA");
+  static_assert(PM >= 1 && OFF_MB % 8 == 0, "merge staging");
+  static_assert(FP8 || (OFF_FX % 8 == 0 && OFF_FX + FX_T * 4 + 8 <= OFF_MB), "the position word lies inside FX");
 };
 
 // Largest number of warps per CTA of any instantiation (sizes the partials).
 constexpr int kMaxWarpsPerCta = 12;
 
-// Fewest retained slots a warp is given (two tiles; bounds the number of
-// partials when the cache is small).  Small caches are latency-bound per warp,
-// so they are spread over as many warps as this allows.
+// Fewest tiles a warp is given (bounds the number of partials when the cache
+// is small).  Small caches are latency-bound per warp, so they are spread over
+// as many warps as this allows.  kMinSlotsPerWarp sizes the grid on the host
+// (two tiles of the 16-slot kernels).
+constexpr int kMinTilesPerWarp = 2;
 constexpr int kMinSlotsPerWarp = 32;
 
 struct DecodeArgs {
@@ -108,7 +125,7 @@ struct DecodeArgs {
   const uint16_t* q;  // bf16 [B][Hq][D]
   float* out;         // fp32 [B][Hq][D]
   float* part_acc;    // [entries][G][D]
-  float* part_ml;     // [entries][G][2]
+  float* part_ml;     // [entries][MLS]: (max, sum) of each of the G heads, padded to 16 bytes
   int32_t* head_cnt;  // [NH * nsplit] arrival counters of split (virtual) heads; zero between calls
   int32_t* err;
   int NH, Hkv, cap;
@@ -122,11 +139,11 @@ struct DecodeArgs {
   int Gq, nsplit;
   // Fused step only (decode_kernel<D, G, true>, dms_step): the new token of
   // position t is appended in the same launch.  `len` is then the base of the
-  // double-buffered lengths [2][NH] (see CacheView): the kernel decodes over
-  // the lengths after the token and writes those, the token's ring entry, slot
-  // map entry and K/V row into the other halves of the double-buffered state,
-  // which no CTA reads.  The position t comes from `t`, or, when t_dev is set
-  // (a step replayed from a CUDA graph), from device memory.
+  // lengths [3][NH] (see CacheView): the kernel decodes over the lengths after
+  // the token and writes those, the token's ring entry, slot map entry and K/V
+  // row into generations of the state that no CTA of the launch reads.  The
+  // position t comes from `t`, or, when t_dev is set (a step replayed from a
+  // CUDA graph), from device memory.
   const uint4* k_new;     // [NH][D/8] the new token's K and V
   const uint4* v_new;
   const float* logit_new;  // [NH]
@@ -139,6 +156,16 @@ struct DecodeArgs {
   const int64_t* t_dev;   // graph-replayed steps: the cache's position in device memory
   int64_t t;
   int w;
+  // Fused step only: 1 when the launch may run its prologue (length scan, work
+  // split) and start its first tile copies before the previous launch in the
+  // stream has finished (programmatic dependent launch).  Everything it reads
+  // before its grid-dependency wait was then written by earlier launches: the
+  // lengths after t - 1 appends, the ring entries of positions t - 1 - w and
+  // t - w (w >= 2), the position word (never written by the launch just before
+  // this one), and pool rows other than the one the previous token went to.
+  // The host sets it only when the previous call that advanced the cache added
+  // exactly one token (so generation t - 1 of the lengths is intact).
+  int early;
 };
 
 // The new token's slot in head x for the fused step at position t: the slot of
@@ -156,7 +183,7 @@ __device__ __forceinline__ int fused_new_slot(const DecodeArgs& a, int64_t t, in
 // Not inlined: the slot lookup of a head beyond the first FX_HEADS of a warp's
 // range (rare), kept out of the decode loop's code.
 static __device__ __noinline__ int fused_new_slot_far(const DecodeArgs& a, int64_t t, int x) {
-  return fused_new_slot(a, t, x, a.len[(t & 1) * a.NH + x]);
+  return fused_new_slot(a, t, x, a.len[len_gen(t) * a.NH + x]);
 }
 
 // Fused step, not inlined (once per head, in the warp whose tile holds the new
@@ -176,37 +203,81 @@ static __device__ __noinline__ void patch_new_row(const DecodeArgs& a, uint4* Kt
   __syncwarp();
 }
 
+// Fused step started early (DecodeArgs::early): head x's state as the step
+// sees it, derived without reading anything the previous step wrote.  From
+// the lengths after t - 1 appends and the ring entries of t - 1 - w and t - w:
+// the slot the previous step's token (position t - 1) went to, the slot of
+// this step's token (position t), and the length after this step's append.
+// The same rule as append_bookkeeping, applied twice.
+struct EarlyHead {
+  int L;       // retained length after t + 1 appends
+  int s_new;   // slot of token t, -1 if the cache is full
+  int s_prev;  // slot of token t - 1, -1 if it was not stored
+};
+
+__device__ __forceinline__ EarlyHead early_head(const DecodeArgs& a, int64_t t, int x) {
+  const int L1 = __ldcg(a.len + len_gen(t - 1) * a.NH + x);
+  int f1 = 0, s1 = 0, f0 = 0, s0 = 0;
+  if (t - 1 >= a.w) {
+    const size_t e = ring_index(a.NH, a.w, x, t - 1 - a.w);
+    f1 = __ldcg(a.ring_flag + e);
+    s1 = __ldcg(a.ring_slot + e);
+  }
+  if (t >= a.w) {
+    const size_t e = ring_index(a.NH, a.w, x, t - a.w);
+    f0 = __ldcg(a.ring_flag + e);
+    s0 = __ldcg(a.ring_slot + e);
+  }
+  EarlyHead h;
+  h.s_prev = f1 ? s1 : (L1 < a.cap ? L1 : -1);
+  const int L2 = (f1 || L1 >= a.cap) ? L1 : L1 + 1;
+  h.s_new = f0 ? s0 : (L2 < a.cap ? L2 : -1);
+  h.L = (f0 || L2 >= a.cap) ? L2 : L2 + 1;
+  return h;
+}
+
 // Retained length of head x as this launch decodes it (fused: after the
 // append of position t).
 template <bool FUSED>
 __device__ __forceinline__ int decode_len(const DecodeArgs& a, int64_t t, int x) {
   if constexpr (FUSED) {
-    const int L = a.len[(t & 1) * a.NH + x];
+    if (a.early) return early_head(a, t, x).L;
+    const int L = a.len[len_gen(t) * a.NH + x];
     const bool retire = t >= a.w && a.ring_flag[ring_index(a.NH, a.w, x, t - a.w)] != 0;
     return (!retire && L < a.cap) ? L + 1 : L;
   }
   return a.len[x];
 }
 
-// Retained-slot iterator over one warp's global range [A, E).
+// Tiles of TK slots in a head of L retained slots (the last one partial).
+template <int TK>
+__host__ __device__ __forceinline__ int tiles_of(int L) { return (L + TK - 1) / TK; }
+
+// Retained-slot iterator over one warp's global range [A, E) of tiles: the
+// heads' tiles concatenated, so every warp range starts and ends on a tile
+// boundary of its heads and holds the same number of tiles (to within one).
+template <int TK>
 struct TileIter {
   int i;      // head
   int L;      // retained length of head i
   int s;      // next slot in head i
   int send;   // end of this warp's slots in head i
-  int64_t P;  // global index of slot 0 of head i
+  int64_t P;  // global index of tile 0 of head i
   int64_t E;
   bool valid;
   bool first;  // next tile opens a new segment (head)
 
+  __device__ __forceinline__ void set_end() {
+    send = static_cast<int>(min(static_cast<int64_t>(L), (E - P) * TK));
+  }
   template <typename LenF>
   __device__ __forceinline__ void start(const LenF& len, int i0, int64_t P0, int64_t A, int64_t E_) {
     i = i0;
     P = P0;
     E = E_;
     L = len(i0);
-    s = static_cast<int>(A - P0);
-    send = static_cast<int>(min(E, P0 + L) - P0);
+    s = static_cast<int>(A - P0) * TK;
+    set_end();
     valid = s < send;
     first = true;
   }
@@ -215,7 +286,7 @@ struct TileIter {
     s += cnt;
     first = false;
     if (s < send) return;
-    P += L;
+    P += tiles_of<TK>(L);
     ++i;
     while (P < E && i < NH) {
       L = len(i);
@@ -227,7 +298,7 @@ struct TileIter {
       return;
     }
     s = 0;
-    send = static_cast<int>(min(E, P + L) - P);
+    set_end();
     first = true;
   }
 };
@@ -274,79 +345,93 @@ __device__ __forceinline__ void scan_lengths(const LenF& len, int NH, int* pre) 
   __syncthreads();
 }
 
+// Arrival counts of split heads.  A warp writes its partial, synchronises
+// (__syncwarp), and lane 0 adds its arrival with release semantics at GPU
+// scope, which publishes the whole warp's partial; the arrival that completes
+// the count also acquires the others' partials.
+__device__ __forceinline__ int arrive_acq_rel(int32_t* cnt) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(cnt) : "memory");
+  return old;
+}
+__device__ __forceinline__ int arrive_release(int32_t* cnt) {
+  int old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(cnt) : "memory");
+  return old;
+}
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acquire.gpu;" ::: "memory"); }
+
 // Merge the nseg partials (max m, sum l, unnormalised acc) of one head, stored
 // at consecutive partial indices base, base + 1, ..., and write the normalised
-// output (outp already offset by lane * EL).  Partials written by other SMs are
-// read from L2 (ld.global.cg).  Pass 1 reduces (max, sum) with the segments
-// spread over the lanes, each lane keeping its first segment's values; pass 2
-// takes 32 segments at a time, each lane computing one segment's weight,
-// broadcast by shuffles while the accumulators' loads of several segments are
-// in flight together.
-template <int D, int G>
-__device__ __forceinline__ void merge_partials(const DecodeArgs& a, size_t base, int nseg, float* outp, int lane) {
-  constexpr int EL = D / 32;
-  const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
+// output (outp already offset by lane * EL).  The partials are staged into
+// shared memory (`stage`, the warp's free tile buffers) by bulk copies of PM
+// partials at a time -- one round trip to L2 for a typical head -- and folded
+// in with a running max per query head.  The caller has acquired the partials
+// (fence after the arrival count); the proxy fence orders those generic-proxy
+// writes before the async-proxy reads of the bulk copy.  Returns false if a
+// copy did not complete within the time limit.
+template <typename Sh>
+__device__ __forceinline__ bool merge_partials(const DecodeArgs& a, size_t base, int nseg, float* outp, int lane,
+                                               uint8_t* stage, uint64_t* mbar, uint32_t& mphase) {
+  constexpr int G = Sh::G, D = Sh::D, EL = D / 32, MLS = Sh::MLS, PM = Sh::PM;
   float M[G], L[G];
+  float2 acc[G][EL / 2];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     M[g] = -INFINITY;
     L[g] = 0.f;
-  }
-  float2 v0[G];  // this lane's segment among the first 32, kept for pass 2
-  for (int k = lane; k < nseg; k += 32) {
-    float2 v[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) v[g] = __ldcg(ml + (base + k) * G + g);
-    if (k == lane) {
-#pragma unroll
-      for (int g = 0; g < G; ++g) v0[g] = v[g];
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float mn = fmaxf(M[g], v[g].x);
-      L[g] = L[g] * fast_exp2(M[g] - mn) + v[g].y * fast_exp2(v[g].x - mn);
-      M[g] = mn;
-    }
-  }
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float Mo = __shfl_xor_sync(0xffffffffu, M[g], off);
-      const float Lo = __shfl_xor_sync(0xffffffffu, L[g], off);
-      const float mn = fmaxf(M[g], Mo);
-      if (mn != -INFINITY) {
-        L[g] = L[g] * fast_exp2(M[g] - mn) + Lo * fast_exp2(Mo - mn);
-        M[g] = mn;
-      }
-    }
-  }
-  float2 acc[G][EL / 2];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
 #pragma unroll
     for (int e = 0; e < EL / 2; ++e) acc[g][e] = make_float2(0.f, 0.f);
   }
-  for (int kb = 0; kb < nseg; kb += 32) {
-    float wv[G];
-    const int k = kb + lane;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float mk = kb == 0 ? v0[g].x : (k < nseg ? __ldcg(ml + (base + k) * G + g).x : 0.f);
-      wv[g] = k < nseg ? fast_exp2(mk - M[g]) : 0.f;
+  if (lane == 0) asm volatile("fence.proxy.async;" ::: "memory");
+  const float* sacc = reinterpret_cast<const float*>(stage);
+  const float* sml = reinterpret_cast<const float*>(stage + PM * G * D * 4);
+  for (int k0 = 0; k0 < nseg; k0 += PM) {
+    const int n = min(PM, nseg - k0);
+    if (lane == 0) {
+      const uint32_t ab = static_cast<uint32_t>(n * G * D * 4), mb = static_cast<uint32_t>(n * MLS * 4);
+      mbar_arrive_expect_tx(mbar, ab + mb);
+      bulk_copy_g2s(stage, a.part_acc + (base + k0) * G * D, ab, mbar);
+      bulk_copy_g2s(stage + PM * G * D * 4, a.part_ml + (base + k0) * MLS, mb, mbar);
     }
-    const int n = min(32, nseg - kb);
-#pragma unroll 4
-    for (int j = 0; j < n; ++j) {
-      const size_t kk = base + kb + j;
+    if (!mbar_wait(mbar, mphase)) {
+      (void)mbar_wait(mbar, mphase);  // give the copy in flight a second bounded wait before leaving
+      return false;
+    }
+    mphase ^= 1u;
+    float mt[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float wk = __shfl_sync(0xffffffffu, wv[g], j);
-        const float2* src = reinterpret_cast<const float2*>(a.part_acc + (kk * G + g) * D + lane * EL);
+    for (int g = 0; g < G; ++g) mt[g] = M[g];
 #pragma unroll
-        for (int e = 0; e < EL / 2; ++e) acc[g][e] = __ffma2_rn(make_float2(wk, wk), __ldcg(src + e), acc[g][e]);
+    for (int j = 0; j < PM; ++j) {
+      if (j < n) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) mt[g] = fmaxf(mt[g], sml[j * MLS + 2 * g]);
       }
     }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float sc = fast_exp2(M[g] - mt[g]);
+      L[g] *= sc;
+#pragma unroll
+      for (int e = 0; e < EL / 2; ++e) acc[g][e] = __fmul2_rn(acc[g][e], make_float2(sc, sc));
+      M[g] = mt[g];
+    }
+#pragma unroll
+    for (int j = 0; j < PM; ++j) {
+      if (j < n) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float2 mlj = *reinterpret_cast<const float2*>(sml + j * MLS + 2 * g);
+          const float wj = fast_exp2(mlj.x - mt[g]);
+          L[g] = fmaf(wj, mlj.y, L[g]);
+          const float2* src = reinterpret_cast<const float2*>(sacc + (j * G + g) * D + lane * EL);
+#pragma unroll
+          for (int e = 0; e < EL / 2; ++e) acc[g][e] = __ffma2_rn(make_float2(wj, wj), src[e], acc[g][e]);
+        }
+      }
+    }
+    __syncwarp();
   }
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -355,6 +440,7 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, size_t base,
     for (int e = 0; e < EL / 2; ++e)
       reinterpret_cast<float2*>(outp + g * D)[e] = make_float2(acc[g][e].x * inv, acc[g][e].y * inv);
   }
+  return true;
 }
 
 template <int D, int G, bool FUSED, int KVF = kKvBf16>
@@ -367,9 +453,15 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   extern __shared__ __align__(1024) uint8_t smem[];
 
   // Launched as a programmatic dependent of the previous kernel: everything the
-  // previous kernels wrote is visible after this wait.
-  griddep_wait();
-  griddep_launch_dependents();
+  // previous kernels wrote is visible after griddep_wait.  A fused step started
+  // early (a.early) first runs its prologue and issues its first tile copies
+  // from state that earlier launches wrote (see DecodeArgs::early), and waits
+  // before it reads any input or writes anything.
+  const bool early = FUSED && a.early != 0;
+  if (!early) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
 
   // ---- prologue: prefix sums of the retained lengths, warp ranges ----
   const int wl = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -387,68 +479,92 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   auto head_group = [&](int v) { return v >= a.NH ? 1 : 0; };
   int* pre = reinterpret_cast<int*>(smem);  // [NV + 1]; aliases the warp regions until the barrier below
   int* sn = pre + NV + 1;                   // fused step: [NH] the new token's slot in each KV head
+  int* sp = sn + a.NH;                      // fused step started early: [NH] the previous token's slot
+  int* ln = sp + a.NH;                      // fused step: [NH] each KV head's length after the append
   // Fused step: warp x of the grid appends the token to head x (and x + nwarps,
   // ...).  Its row chunk (K for lanes < CH, V for lanes CH .. 2 CH - 1) and
-  // logit are loaded now, in flight during the scan.
+  // logit are loaded now, in flight during the scan (not when started early:
+  // the inputs may come from the launch just before).
   uint4 own_row = make_uint4(0u, 0u, 0u, 0u);
   float own_logit = 0.f;
   if constexpr (FUSED) {
-    if (wg < a.NH) {
+    if (!early && wg < a.NH) {
       if (lane < 2 * CH)
         own_row = __ldg((lane < CH ? a.k_new : a.v_new) + static_cast<size_t>(wg) * CH + (lane % CH));
       own_logit = __ldg(a.logit_new + wg);
     }
   }
-  // The scan reads each head's length (and, fused, the ring entry of t - w) once;
-  // the fused scan also records the new token's slot in sn.
+  // The scan reads each head's length (and, fused, the ring entry of t - w) once
+  // and sums its tiles; the fused scan also records the new token's slot in sn
+  // and the length after the append in ln.
   auto scanf = [&](int v) {
     const int x = real_head(v);
     if constexpr (FUSED) {
-      const int L = a.len[(t_step & 1) * a.NH + x];
+      if (early) {
+        const EarlyHead eh = early_head(a, t_step, x);
+        if (v < a.NH) {
+          sn[x] = eh.s_new;
+          sp[x] = eh.s_prev;
+          ln[x] = eh.L;
+        }
+        return tiles_of<TK>(eh.L);
+      }
+      const int L = a.len[len_gen(t_step) * a.NH + x];
       int fl = 0, sl = 0;
       if (t_step >= a.w) {
         const size_t e = ring_index(a.NH, a.w, x, t_step - a.w);
         fl = a.ring_flag[e];
         sl = a.ring_slot[e];
       }
-      if (v < a.NH) sn[x] = fl ? sl : (L < a.cap ? L : -1);
-      return (fl || L >= a.cap) ? L : L + 1;
+      const int L3 = (fl || L >= a.cap) ? L : L + 1;
+      if (v < a.NH) {
+        sn[x] = fl ? sl : (L < a.cap ? L : -1);
+        ln[x] = L3;
+      }
+      return tiles_of<TK>(L3);
     } else {
-      return a.len[x];
+      return tiles_of<TK>(a.len[x]);
     }
   };
   scan_lengths(scanf, NV, pre);
+  // Fused step: the bookkeeping and row of the new token in head i (length
+  // after the append L_i, slot s_new, -1 if the cache is full).  None of it is
+  // read by this launch: the next generations of the lengths and the ring, the
+  // slot map, and a pool row that every tile copy skips (the new row is taken
+  // from the input).
+  auto append_head = [&](int i, int s_new, int L_i, uint4 rowc, float lg) {
+    if (lane == 0) {
+      a.len_w[len_gen(t_step + 1) * a.NH + i] = L_i;
+      const size_t e = ring_index(a.NH, a.w, i, t_step);
+      a.ring_slot[e] = s_new;
+      a.ring_flag[e] = (s_new >= 0 && lg > 0.0f) ? 1 : 0;
+      if (s_new >= 0) a.slot_pos[static_cast<size_t>(i) * a.cap + s_new] = static_cast<int32_t>(t_step);
+      else atomicOr(a.err, kErrBitCapacity);
+    }
+    if (s_new >= 0) {
+      const size_t row = (static_cast<size_t>(i) * a.cap + s_new) * CH;
+      if (lane < CH) a.K_w[row + (lane ^ (s_new & 7))] = rowc;
+      else if (lane < 2 * CH) a.V_w[row + lane - CH] = rowc;
+    }
+  };
+  auto load_new_row = [&](int i) {
+    uint4 rowc = make_uint4(0u, 0u, 0u, 0u);
+    if (lane < 2 * CH) rowc = __ldg((lane < CH ? a.k_new : a.v_new) + static_cast<size_t>(i) * CH + (lane % CH));
+    return rowc;
+  };
   if constexpr (FUSED) {
-    // Bookkeeping and row of the new token; none of it is read by this launch
-    // (other halves of the double-buffered state, the slot map, and a pool row
-    // that every tile copy skips: the new row is copied from the input).
-    for (int64_t x = wg; x < a.NH; x += nwarps) {
-      const int i = static_cast<int>(x);
-      const int s_new = sn[i];
-      uint4 rowc = own_row;
-      float lg = own_logit;
-      if (x != wg) {
-        if (lane < 2 * CH) rowc = __ldg((lane < CH ? a.k_new : a.v_new) + static_cast<size_t>(i) * CH + (lane % CH));
-        lg = __ldg(a.logit_new + i);
-      }
-      if (lane == 0) {
-        a.len_w[((t_step + 1) & 1) * a.NH + i] = pre[i + 1] - pre[i];
-        const size_t e = ring_index(a.NH, a.w, i, t_step);
-        a.ring_slot[e] = s_new;
-        a.ring_flag[e] = (s_new >= 0 && lg > 0.0f) ? 1 : 0;
-        if (s_new >= 0) a.slot_pos[static_cast<size_t>(i) * a.cap + s_new] = static_cast<int32_t>(t_step);
-        else atomicOr(a.err, kErrBitCapacity);
-      }
-      if (s_new >= 0) {
-        const size_t row = (static_cast<size_t>(i) * a.cap + s_new) * CH;
-        if (lane < CH) a.K_w[row + (lane ^ (s_new & 7))] = rowc;
-        else if (lane < 2 * CH) a.V_w[row + lane - CH] = rowc;
+    if (!early) {
+      for (int64_t x = wg; x < a.NH; x += nwarps) {
+        const int i = static_cast<int>(x);
+        const bool own = x == wg;
+        append_head(i, sn[i], ln[i], own ? own_row : load_new_row(i),
+                    own ? own_logit : __ldg(a.logit_new + i));
       }
     }
   }
-  const int64_t S = pre[NV];
+  const int64_t S = pre[NV];  // tiles of all heads
   int64_t Pe = nwarps;
-  if (S / kMinSlotsPerWarp < Pe) Pe = S / kMinSlotsPerWarp;
+  if (S / kMinTilesPerWarp < Pe) Pe = S / kMinTilesPerWarp;
   if (Pe < 1) Pe = 1;
   const bool active = S > 0 && wg < Pe;
   int64_t A = 0, E = 0, P0 = 0;
@@ -465,14 +581,23 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
     P0 = pre[lo];
   }
   // Fused step: the new token's slots of heads i0, i0 + 1, ... (read before the
-  // barrier, which ends the prefix sums' lease on the warp regions).
-  int snl = -1;
+  // barrier, which ends the prefix sums' lease on the warp regions).  Started
+  // early: also the slot of the previous step's token in head i0 (its tile is
+  // not copied before the wait), and this warp's own head to append.
+  int snl = -1, sprev0 = -1, own_sn = -1, own_L = 0;
   if constexpr (FUSED) {
     if (active && lane < Sh::FX_HEADS && i0 + lane < NV) snl = sn[real_head(i0 + lane)];
+    if (early) {
+      if (active) sprev0 = sp[real_head(i0)];
+      if (wg < a.NH) {
+        own_sn = sn[wg];
+        own_L = ln[wg];
+      }
+    }
   }
   __syncthreads();
 
-  if (!active) return;
+  if (!active && !early) return;
 
   // ---- per-warp shared memory ----
   uint8_t* wbase = smem + wl * Sh::WARP_BYTES;
@@ -482,16 +607,23 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   float* pb = reinterpret_cast<float*>(wbase + Sh::OFF_P);
   uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + Sh::OFF_BAR);  // [NST] tiles
   int* fx = reinterpret_cast<int*>(wbase + Sh::OFF_FX);               // fused-step state
-  if (lane == 0) {
-    for (int x = 0; x < NST; ++x) mbar_init(&bars[x], 1);
-    fence_barrier_init();
-  }
-  if constexpr (FUSED) {
-    if (lane < Sh::FX_HEADS) fx[lane] = snl;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(wbase + Sh::OFF_MB);   // merge copies
+  int* def = reinterpret_cast<int*>(wbase + Sh::OFF_DEF);              // deferred arrival, merge phase
+  if (active) {
     if (lane == 0) {
-      fx[Sh::FX_I0] = i0;
-      fx[Sh::FX_SEG] = -1;
-      *reinterpret_cast<int64_t*>(fx + Sh::FX_T) = t_step;
+      for (int x = 0; x < NST; ++x) mbar_init(&bars[x], 1);
+      mbar_init(mbar, 1);
+      fence_barrier_init();
+      def[0] = -1;
+      def[4] = 0;
+    }
+    if constexpr (FUSED) {
+      if (lane < Sh::FX_HEADS) fx[lane] = snl;
+      if (lane == 0) {
+        fx[Sh::FX_I0] = i0;
+        fx[Sh::FX_SEG] = -1;
+        *reinterpret_cast<int64_t*>(fx + Sh::FX_T) = t_step;
+      }
     }
   }
   __syncwarp();
@@ -503,12 +635,37 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   };
 
   const int Hq = a.Hkv * a.Gq;
-  TileIter is{}, cs{};
-  is.start(lenf, i0, P0, A, E);
+  TileIter<TK> is{}, cs{};
+  if (active) is.start(lenf, i0, P0, A, E);
   cs = is;
   int n_issued = 0, n_cons = 0, nq_issued = 0, nq_conv = 0;
   constexpr int QV = Sh::QV;
   uint4 qpre[QV];  // bf16 q rows of the next segment, 8 elements per chunk
+
+  // The K and V tile copies of the iterator's next tile (lane 0).
+  auto issue_tile = [&](int cnt) {
+    if (lane == 0) {
+      const int buf = n_issued % NST;
+      const uint32_t kbytes = static_cast<uint32_t>(cnt * ROWB_K), vbytes = static_cast<uint32_t>(cnt * ROWB_V);
+      const size_t row = static_cast<size_t>(real_head(is.i)) * a.cap + is.s;
+      mbar_arrive_expect_tx(&bars[buf], kbytes + vbytes);
+      bulk_copy_g2s(Ks + buf * TILEB_K, a.K + row * Sh::KU4, kbytes, &bars[buf]);
+      bulk_copy_g2s(Vs + buf * TILEB_V, a.V + row * Sh::VU4, vbytes, &bars[buf]);
+    }
+  };
+  // The G query rows of virtual head v into qpre.
+  auto load_q = [&](int v) {
+    const int x = real_head(v);
+    const int b = x / a.Hkv, h = x - (x / a.Hkv) * a.Hkv;
+    const uint4* qsrc =
+        reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * Hq + h * a.Gq + head_group(v) * G) * D);
+#pragma unroll
+    for (int u = 0; u < QV; ++u) {
+      const int y = lane + 32 * u;
+      if (y < G * D / 8) qpre[u] = __ldg(qsrc + y);
+    }
+    ++nq_issued;
+  };
 
   // Issue tiles ahead while buffers are free.  A segment's first tile also
   // starts the load of that segment's q into qpre, which must have been
@@ -517,36 +674,68 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
     while (is.valid && n_issued < n_cons + NST) {
       if (is.first && nq_issued != nq_conv) break;
       const int cnt = min(TK, is.send - is.s);
-      const int buf = n_issued % NST;
-      if (lane == 0) {
-        const uint32_t kbytes = static_cast<uint32_t>(cnt * ROWB_K), vbytes = static_cast<uint32_t>(cnt * ROWB_V);
-        const size_t row = static_cast<size_t>(real_head(is.i)) * a.cap + is.s;
-        mbar_arrive_expect_tx(&bars[buf], kbytes + vbytes);
-        bulk_copy_g2s(Ks + buf * TILEB_K, a.K + row * Sh::KU4, kbytes, &bars[buf]);
-        bulk_copy_g2s(Vs + buf * TILEB_V, a.V + row * Sh::VU4, vbytes, &bars[buf]);
-      }
-      if (is.first) {
-        const int x = real_head(is.i);
-        const int b = x / a.Hkv, h = x - (x / a.Hkv) * a.Hkv;
-        const uint4* qsrc =
-            reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * Hq + h * a.Gq + head_group(is.i) * G) * D);
-#pragma unroll
-        for (int v = 0; v < QV; ++v) {
-          const int x = lane + 32 * v;
-          if (x < G * D / 8) qpre[v] = __ldg(qsrc + x);
-        }
-        ++nq_issued;
-      }
+      issue_tile(cnt);
+      if (is.first) load_q(is.i);
       ++n_issued;
       is.advance(lenf, NV, cnt);
     }
   };
+
+  if constexpr (FUSED) {
+    if (early) {
+      // Before the wait: up to NST tiles of the first head, stopping at the tile
+      // that holds the previous step's token (its row may still be in flight).
+      if (active) {
+        while (is.valid && n_issued < NST && is.i == i0) {
+          const int cnt = min(TK, is.send - is.s);
+          if (static_cast<unsigned>(sprev0 - is.s) < static_cast<unsigned>(cnt)) break;
+          issue_tile(cnt);
+          ++n_issued;
+          is.advance(lenf, NV, cnt);
+        }
+      }
+      griddep_wait();
+      griddep_launch_dependents();
+      for (int64_t x = wg; x < a.NH; x += nwarps) {
+        const int i = static_cast<int>(x);
+        if (x == wg) {
+          append_head(i, own_sn, own_L, load_new_row(i), __ldg(a.logit_new + i));
+        } else {
+          const EarlyHead eh = early_head(a, t_step, i);
+          append_head(i, eh.s_new, eh.L, load_new_row(i), __ldg(a.logit_new + i));
+        }
+      }
+      if (!active) return;
+      if (n_issued > 0) load_q(i0);  // the first segment's q, now that the inputs are visible
+    }
+  }
 
   // Latch a timeout, then wait (bounded) for this warp's copies in flight.
   auto fail_and_drain = [&]() {
     if (lane == 0) atomicOr(a.err, kErrBitTimeout);
     for (int k = n_cons; k < n_issued; ++k) (void)mbar_wait(&bars[k % NST], (k / NST) & 1);
   };
+
+  // Merge of split head v's nseg partials from index base into its output (the
+  // last arriver); a copy that timed out latches the error.
+  auto merge_head = [&](int v, size_t base, int nseg) {
+    const int x = real_head(v);
+    const int b = x / a.Hkv, h = x - b * a.Hkv;
+    float* outp = a.out + (static_cast<size_t>(b) * Hq + h * a.Gq + head_group(v) * G) * D + lane * EL;
+    uint32_t ph = static_cast<uint32_t>(def[4]);
+    const bool ok = merge_partials<Sh>(a, base, nseg, outp, lane, wbase, mbar, ph);
+    __syncwarp();
+    if (lane == 0) {
+      def[4] = static_cast<int>(ph);
+      a.head_cnt[v] = 0;  // for the next call
+      if (!ok) atomicOr(a.err, kErrBitTimeout);
+    }
+    __syncwarp();
+  };
+  // The arrival count of the warp's first segment when later segments follow
+  // (lane 0; -1 when none is pending).  It is read only after the next tile has
+  // landed, so the stream never waits on it.
+  int pend = -1;
 
   // QK lane roles: two lanes per slot, each over half of the head dim.
   const int r = lane & 15, hf = lane >> 4;
@@ -604,6 +793,10 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
     if (n_issued <= n_cons || !mbar_wait(&bars[buf], (n_cons / NST) & 1)) {
       fail_and_drain();
       return;
+    }
+    if (pend >= 0) {
+      def[3] = pend;
+      pend = -1;
     }
 
     if constexpr (FUSED) {
@@ -833,9 +1026,9 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
       const int x = real_head(seg_i);
       const int b = x / a.Hkv, h = x - b * a.Hkv;
       float* outp = a.out + (static_cast<size_t>(b) * Hq + h * a.Gq + head_group(seg_i) * G) * D + lane * EL;
-      // Warps holding the first and the last slot of this head.
+      // Warps holding the first and the last tile of this head.
       const int64_t w0 = ((seg_P + 1) * Pe - 1) / S;
-      const int64_t w1 = ((seg_P + seg_L) * Pe - 1) / S;
+      const int64_t w1 = ((seg_P + tiles_of<TK>(seg_L)) * Pe - 1) / S;
       if (w0 == w1) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -863,24 +1056,38 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
               ll = l[g];
             }
           }
-          reinterpret_cast<float2*>(a.part_ml)[idx * G + lane] = make_float2(mm, ll);
+          reinterpret_cast<float2*>(a.part_ml + idx * Sh::MLS)[lane] = make_float2(mm, ll);
         }
         // Release the partial, then count this arrival; the last of the head's
-        // nseg warps merges (acquire) and resets the counter.
+        // nseg warps merges (acquire) and resets the counter.  Only a warp's first
+        // segment can be split and followed by more: its count is looked at once
+        // the range is done (the other pieces of that head end their warps'
+        // ranges, so it is rarely the last), and the stream goes on meanwhile.
         const int nseg = static_cast<int>(w1 - w0) + 1;
-        __threadfence();
         __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomicAdd(a.head_cnt + seg_i, 1) == nseg - 1;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence();
-          merge_partials<D, G>(a, static_cast<size_t>(w0 + seg_i), nseg, outp, lane);
-          if (lane == 0) a.head_cnt[seg_i] = 0;
+        if (cs.valid) {
+          if (lane == 0) {
+            def[0] = seg_i;
+            def[1] = static_cast<int>(w0 + seg_i);
+            def[2] = nseg;
+            pend = arrive_release(a.head_cnt + seg_i);
+          }
+        } else {
+          int last = 0;
+          if (lane == 0) last = arrive_acq_rel(a.head_cnt + seg_i) == nseg - 1;
+          last = __shfl_sync(0xffffffffu, last, 0);
+          if (last) merge_head(seg_i, static_cast<size_t>(w0 + seg_i), nseg);
         }
       }
     }
     try_issue();
+  }
+  // The deferred first segment: merge it if this warp's arrival was the last.
+  if (pend >= 0) def[3] = pend;
+  __syncwarp();
+  if (def[0] >= 0 && def[3] == def[2] - 1) {
+    if (lane == 0) fence_acquire_gpu();
+    merge_head(def[0], static_cast<size_t>(def[1]), def[2]);
   }
 }
 

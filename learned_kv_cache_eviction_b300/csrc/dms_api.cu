@@ -22,6 +22,10 @@ struct dms_cache {
   int B, H, cap, D, w, NH;
   int kvf;  // DMS_KV_BF16 or DMS_KV_FP8_E4M3
   int64_t t;
+  // The last call that advanced t added exactly one token, so the lengths after
+  // t - 1 appends are still in their generation: the next fused step may then
+  // start before the previous launch has finished (DecodeArgs::early).
+  bool single_prev;
   int device;
   int num_sms;
   dms::CacheView view;
@@ -109,13 +113,20 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
 
 // The new token of a fused step (dms_step): its K, V rows and eviction logit;
 // t_dev set when the launch is captured into a CUDA graph (the position is
-// then read from device memory at replay).
+// then read from device memory at replay); early: the launch may start before
+// the previous one has finished (DecodeArgs::early).
 struct StepInput {
   const uint4* k;
   const uint4* v;
   const float* logit;
   const int64_t* t_dev;
+  bool early;
 };
+
+// May the fused step of cache c at its current position start early?  Needs
+// the lengths after t - 1 appends (the last advance added one token) and ring
+// entries of t - 1 - w and t - w that the previous step does not write (w >= 2).
+bool step_can_start_early(const dms_cache* c) { return c->w >= 2 && c->t >= 1 && c->single_prev; }
 
 // Decode launch.  Plain (FUSED false): attention of q over the cache as it
 // stands at position c->t.  Fused (FUSED true, `in` set): the token of
@@ -145,8 +156,8 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
   using Sh = dms::DecodeShape<D, G, KVF>;
   if (decode_attr<D, G, FUSED, KVF>(c) != DMS_OK) return DMS_ERR_CUDA;
   const int64_t NV = static_cast<int64_t>(c->NH) * nsplit;
-  // The prologue's prefix sums (and, fused, each head's new slot) fit in shared memory.
-  if ((NV + 1 + (FUSED ? c->NH : 0)) * 4 > Sh::SMEM) return DMS_ERR_INVALID_ARG;
+  // The prologue's prefix sums (and, fused, each head's new and previous slot and length) fit in shared memory.
+  if ((NV + 1 + (FUSED ? 3 * c->NH : 0)) * 4 > Sh::SMEM) return DMS_ERR_INVALID_ARG;
   // Upper bound of the retained slots (the exact sum lives on the device); a
   // graph-replayed step runs at positions unknown now, so it takes the capacity.
   const bool graph = FUSED && in != nullptr && in->t_dev != nullptr;
@@ -182,6 +193,7 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
   a.t_dev = nullptr;
   a.t = c->t;
   a.w = c->w;
+  a.early = 0;
   if constexpr (FUSED) {
     a.k_new = in->k;
     a.v_new = in->v;
@@ -192,6 +204,7 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
     a.len = c->view.len;  // both halves: the kernel picks them by the position's parity
     a.len_w = c->view.len;
     a.t_dev = in->t_dev;
+    a.early = in->early ? 1 : 0;
   }
   return launch_pdl(dms::decode_kernel<D, G, FUSED, KVF>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
 }
@@ -322,6 +335,13 @@ struct dms_step_graph {
   cudaGraphExec_t exec = nullptr;
   int64_t** pos = nullptr;  // device array: each cache's position word
   int device = 0;
+  // The buffers bound at capture, for a token step run as per-layer launches
+  // when the graph's early-started layers may not start early (see launch).
+  std::vector<const void*> k, v, q;
+  std::vector<const float*> logit;
+  std::vector<float*> out;
+  float scale = 1.f;
+  int q_heads = 0;
 };
 
 namespace {
@@ -447,6 +467,7 @@ dms_cache_t* dms_cache_create_ex(int batch, int kv_heads, int capacity, int head
   c->NH = static_cast<int>(NH);
   c->kvf = kv_format;
   c->t = 0;
+  c->single_prev = false;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
     cudaGetLastError();
@@ -468,14 +489,14 @@ dms_cache_t* dms_cache_create_ex(int batch, int kv_heads, int capacity, int head
             cudaMalloc(&c->view.slot_pos, nslot * 4) == cudaSuccess &&
             cudaMalloc(&c->view.ring_slot, nring * 4) == cudaSuccess &&
             cudaMalloc(&c->view.ring_flag, nring) == cudaSuccess &&
-            cudaMalloc(&c->view.len, 2 * NH * 4) == cudaSuccess && cudaMalloc(&c->view.err, kAlign) == cudaSuccess &&
+            cudaMalloc(&c->view.len, dms::kLenGens * NH * 4) == cudaSuccess && cudaMalloc(&c->view.err, kAlign) == cudaSuccess &&
             cudaMalloc(&c->part_acc, part_acc) == cudaSuccess && cudaMalloc(&c->part_ml, part_ml) == cudaSuccess &&
             cudaMalloc(&c->head_cnt, 2 * NH * 4) == cudaSuccess &&
             (!fp8 || cudaMalloc(&c->round_buf, RoundLayout(c).total) == cudaSuccess);
   ok = ok && cudaMemset(c->view.K, 0, kpool) == cudaSuccess && cudaMemset(c->view.V, 0, vpool) == cudaSuccess &&
        cudaMemset(c->view.slot_pos, 0xff, nslot * 4) == cudaSuccess &&
        cudaMemset(c->view.ring_slot, 0xff, nring * 4) == cudaSuccess &&
-       cudaMemset(c->view.ring_flag, 0, nring) == cudaSuccess && cudaMemset(c->view.len, 0, 2 * NH * 4) == cudaSuccess &&
+       cudaMemset(c->view.ring_flag, 0, nring) == cudaSuccess && cudaMemset(c->view.len, 0, dms::kLenGens * NH * 4) == cudaSuccess &&
        cudaMemset(c->view.err, 0, kAlign) == cudaSuccess && cudaMemset(c->head_cnt, 0, 2 * NH * 4) == cudaSuccess &&
        cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
@@ -522,7 +543,10 @@ int dms_append(dms_cache_t* c, const void* k, const void* v, const float* evict_
       !device_pointer_ok(evict_logit, c->device))
     return DMS_ERR_INVALID_ARG;
   const int rc = launch_append(c, k, v, evict_logit, static_cast<cudaStream_t>(stream));
-  if (rc == DMS_OK) c->t += 1;
+  if (rc == DMS_OK) {
+    c->t += 1;
+    c->single_prev = true;
+  }
   c->t_dev_synced = false;
   return rc;
 }
@@ -536,7 +560,10 @@ int dms_append_chunk(dms_cache_t* c, const void* k, const void* v, const float* 
   if (!device_pointer_ok(k, c->device) || !device_pointer_ok(v, c->device) || !device_pointer_ok(logits, c->device))
     return DMS_ERR_INVALID_ARG;
   const int rc = launch_append_chunk(c, k, v, logits, chunk, static_cast<cudaStream_t>(stream));
-  if (rc == DMS_OK) c->t += chunk;
+  if (rc == DMS_OK) {
+    c->t += chunk;
+    c->single_prev = chunk == 1;
+  }
   c->t_dev_synced = false;
   return rc;
 }
@@ -557,6 +584,7 @@ int dms_prefill(dms_cache_t* c, const void* q, const void* k, const void* v, con
   if (c->kvf == DMS_KV_FP8_E4M3) {
     // the tensor-core kernel reads bf16 rows; FP8 caches run the definition
     const int rc = prefill_by_rounds(c, q, k, v, logits, chunk, out, scale, q_heads, st);
+    c->single_prev = rc == DMS_OK;  // rounds of single appends
     c->t_dev_synced = false;
     return rc;
   }
@@ -583,7 +611,10 @@ int dms_prefill(dms_cache_t* c, const void* q, const void* k, const void* v, con
   int rc = c->D == 128 ? launch_prefill_d<128>(c, a, G, st) : launch_prefill_d<64>(c, a, G, st);
   if (rc != DMS_OK) return rc;
   rc = launch_append_chunk(c, k, v, logits, chunk, st);
-  if (rc == DMS_OK) c->t += chunk;
+  if (rc == DMS_OK) {
+    c->t += chunk;
+    c->single_prev = chunk == 1;
+  }
   c->t_dev_synced = false;
   return rc;
 }
@@ -623,18 +654,22 @@ int dms_step(dms_cache_t* c, const void* k, const void* v, const float* evict_lo
     int rc = launch_append(c, k, v, evict_logit, st);
     if (rc != DMS_OK) return rc;
     c->t += 1;
+    c->single_prev = true;
     c->t_dev_synced = false;
     return c->D == 128 ? launch_decode_f<128, false>(c, q, out, scale, G, st)
                        : launch_decode_f<64, false>(c, q, out, scale, G, st);
   }
-  // bf16: one launch.  The decode kernel appends the token (into the halves of
-  // the double-buffered state that the step does not read) and attends over
-  // the cache after the append.
-  const StepInput in{static_cast<const uint4*>(k), static_cast<const uint4*>(v), evict_logit, nullptr};
+  // bf16: one launch.  The decode kernel appends the token (into generations of
+  // the state that the step does not read) and attends over the cache after
+  // the append; after a one-token advance it starts before the previous launch
+  // has finished.
+  const StepInput in{static_cast<const uint4*>(k), static_cast<const uint4*>(v), evict_logit, nullptr,
+                     step_can_start_early(c)};
   const int rc = c->D == 128 ? launch_decode_f<128, true>(c, q, out, scale, G, st, &in)
                              : launch_decode_f<64, true>(c, q, out, scale, G, st, &in);
   if (rc != DMS_OK) return rc;
   c->t += 1;
+  c->single_prev = true;
   c->t_dev_synced = false;
   return DMS_OK;
 }
@@ -763,10 +798,14 @@ dms_step_graph_t* dms_step_graph_create(dms_cache_t* const* caches, int n, const
   int rc = DMS_OK;
   if (ok) {
     // One fused step per cache, each reading its position from device memory,
-    // then one node that advances every position.
+    // then one node that advances every position.  Layers after the first
+    // start early (their launch's predecessor is another cache's step, which
+    // writes none of their state); the first waits, since the node before it
+    // writes the position words.
     for (int i = 0; i < n && rc == DMS_OK; ++i) {
       dms_cache* c = caches[i];
-      const StepInput in{static_cast<const uint4*>(k[i]), static_cast<const uint4*>(v[i]), evict_logit[i], c->t_dev};
+      const StepInput in{static_cast<const uint4*>(k[i]), static_cast<const uint4*>(v[i]), evict_logit[i], c->t_dev,
+                         i > 0 && c->w >= 2};
       const int G = q_heads / c->H;
       rc = c->D == 128 ? launch_decode_d<128, true, dms::kKvBf16>(c, q[i], out[i], scale, G, st, &in)
                        : launch_decode_d<64, true, dms::kKvBf16>(c, q[i], out[i], scale, G, st, &in);
@@ -788,6 +827,13 @@ dms_step_graph_t* dms_step_graph_create(dms_cache_t* const* caches, int n, const
     g_last_error = rc == DMS_ERR_INVALID_ARG ? DMS_ERR_INVALID_ARG : DMS_ERR_CUDA;
     return nullptr;
   }
+  sg->k.assign(k, k + n);
+  sg->v.assign(v, v + n);
+  sg->logit.assign(evict_logit, evict_logit + n);
+  sg->q.assign(q, q + n);
+  sg->out.assign(out, out + n);
+  sg->scale = scale;
+  sg->q_heads = q_heads;
   g_last_error = DMS_OK;
   return sg;
 }
@@ -799,6 +845,32 @@ int dms_step_graph_launch(dms_step_graph_t* sg, void* stream) {
   DeviceGuard g(sg->device);
   if (!g.ok) return DMS_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The layers captured to start early need each cache's last advance to have
+  // been one token (true after any replay or dms_step).  Otherwise -- after a
+  // chunk append, or on an empty cache -- this token step runs as one fused
+  // launch per layer, none started early, on the same bound buffers.
+  bool early_ok = true;
+  for (size_t i = 1; i < sg->caches.size(); ++i) {
+    const dms_cache* c = sg->caches[i];
+    if (c->w >= 2 && !step_can_start_early(c)) early_ok = false;
+  }
+  if (!early_ok) {
+    for (size_t i = 0; i < sg->caches.size(); ++i) {
+      dms_cache* c = sg->caches[i];
+      const StepInput in{static_cast<const uint4*>(sg->k[i]), static_cast<const uint4*>(sg->v[i]), sg->logit[i],
+                         nullptr, false};
+      const int G = sg->q_heads / c->H;
+      const int rc = c->D == 128 ? launch_decode_d<128, true, dms::kKvBf16>(c, sg->q[i], sg->out[i], sg->scale, G,
+                                                                           st, &in)
+                                 : launch_decode_d<64, true, dms::kKvBf16>(c, sg->q[i], sg->out[i], sg->scale, G,
+                                                                          st, &in);
+      if (rc != DMS_OK) return rc;
+      c->t += 1;
+      c->single_prev = true;
+      c->t_dev_synced = false;
+    }
+    return DMS_OK;
+  }
   for (dms_cache* c : sg->caches) {
     if (c->t_dev_synced) continue;
     const int rc = launch_pdl(dms::set_position_kernel, dim3(1), dim3(1), 0, st, c->t_dev, c->t);
@@ -809,7 +881,10 @@ int dms_step_graph_launch(dms_step_graph_t* sg, void* stream) {
     cudaGetLastError();
     return DMS_ERR_CUDA;
   }
-  for (dms_cache* c : sg->caches) c->t += 1;
+  for (dms_cache* c : sg->caches) {
+    c->t += 1;
+    c->single_prev = true;
+  }
   return DMS_OK;
 }
 

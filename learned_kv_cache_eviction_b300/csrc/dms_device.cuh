@@ -20,10 +20,14 @@ constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;
 // so that a contiguous bulk copy of consecutive slots into shared memory can
 // be read one row per lane without bank conflicts.  V is stored unpermuted.
 //
-// The lengths and the ring are double-buffered, so that one kernel can read a
-// step's old state from every CTA while it writes the new state (the fused
-// append + decode step): the lengths after t appends are len[t & 1], and the
-// ring entry (slot, mark) of position p is ring[(p / w) & 1][i][p % w].
+// The lengths are kept in three generations and the ring in two, so that one
+// kernel can read a step's old state from every CTA while it writes the new
+// state (the fused append + decode step): the lengths after t appends are
+// len[t % 3], and the ring entry (slot, mark) of position p is
+// ring[(p / w) & 1][i][p % w].  The third generation of lengths lets a fused
+// step start before the previous step has finished: it derives its lengths
+// from generation t - 1, which neither the previous step (writing t) nor
+// itself (writing t + 1) touches.
 //
 // FP8 storage (kvf == kKvFp8): a K row is D E4M3 codes followed by one 16-byte
 // chunk {K scale, V scale, 0, 0} (float32); a V row is D codes.  The K row
@@ -39,15 +43,21 @@ struct CacheView {
   int32_t* slot_pos;   // [NH][cap]
   int32_t* ring_slot;  // [2][NH][w]
   uint8_t* ring_flag;  // [2][NH][w]
-  int32_t* len;        // [2][NH]
+  int32_t* len;        // [3][NH]
   int32_t* err;        // sticky error bits
   int NH, cap, D, w;
   int kvf;  // kKvBf16 or kKvFp8
 };
 
+// Generations of the lengths kept in CacheView::len.
+constexpr int kLenGens = 3;
+
+// Generation holding the lengths after t appends (t >= 0).
+__host__ __device__ __forceinline__ int64_t len_gen(int64_t t) { return t % kLenGens; }
+
 // Lengths after t appends.
 __host__ __device__ __forceinline__ int32_t* len_after(const CacheView& c, int64_t t) {
-  return c.len + (t & 1) * static_cast<int64_t>(c.NH);
+  return c.len + len_gen(t) * static_cast<int64_t>(c.NH);
 }
 
 // Index of the ring entry of position p of head i.

@@ -102,7 +102,7 @@ int run(int dev, int num_sms, unsigned char* scratch, const void* k_pool, const 
   const size_t cnt_off = 256;
   const size_t acc_off = cnt_off + ((static_cast<size_t>(NH) * 4 + 255) / 256) * 256;
   const size_t acc_bytes = entries * G * D * sizeof(float);
-  const size_t ml_bytes = entries * G * 2 * sizeof(float);
+  const size_t ml_bytes = entries * Sh::MLS * sizeof(float);
   if (acc_off + acc_bytes + ml_bytes > kScratchBytes) return DMS_ERR_SCRATCH_LIMIT;
   if (dev < kMaxDevices && !g_attr_done[dev][D == 128][G]) {
     if (cudaFuncSetAttribute(dms::decode_kernel<D, G, false, dms::kKvBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) !=

@@ -394,6 +394,64 @@ def test_step_equals_append_then_decode(case):
     b.close()
 
 
+@pytest.mark.parametrize("case", [
+    # B, Hq, Hkv, D, w, cap, T, logits
+    (4, 16, 4, 128, 16, 700, 640, ("normal", 0.6, 1.0)),  # G 4, window 16
+    (2, 16, 2, 64, 2, 500, 420, ("normal", 0.3, 1.0)),    # G 8 (two groups of 4), d64, window 2
+    (3, 6, 3, 128, 1, 400, 300, ("normal", 0.0, 1.0)),    # window 1: steps never start early
+    (2, 8, 2, 128, 16, 60, 100, ("const", -10.0)),        # the cache fills at t = 60 (capacity error)
+])
+def test_back_to_back_steps_with_mixed_calls(case):
+    """Streams of dms_step calls with no host synchronisation between them, so
+    that each step's early-started prologue and first tile copies run while
+    the previous step is still on the GPU, mixed with the calls that decide
+    whether a step may start early: chunk appends (the next step must not),
+    single appends and plain decodes.  Every output and the final cache state
+    equal, bit for bit, dms_append + dms_decode_attention per token."""
+    B, Hq, Hkv, D, w, cap, T, logits = case
+    wl = _small("b2b", B, Hq, Hkv, D, w, cap, logits, seed=19)
+    k_all, v_all, lg_all = (x.cuda() for x in W.kv_range(wl, 0, 0, T))
+    q_all = W.q_range(wl, 0, 0, T).cuda()
+    a = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
+    b = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
+    T0 = 40
+    for c in (a, b):
+        c.append_chunk(k_all[:, :, :T0].contiguous(), v_all[:, :, :T0].contiguous(), lg_all[:, :, :T0].contiguous())
+    out_a = torch.zeros((T, wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    out_b = torch.zeros_like(out_a)
+    kk = [k_all[:, :, t].contiguous() for t in range(T)]
+    vv = [v_all[:, :, t].contiguous() for t in range(T)]
+    ll = [lg_all[:, :, t].contiguous() for t in range(T)]
+    qq = [q_all[:, :, t].contiguous() for t in range(T)]
+    t = T0
+    while t < T:
+        if t % 97 == 0 and t + 3 <= T:  # a chunk of 3 on both sides; no outputs for those tokens
+            for c in (a, b):
+                c.append_chunk(k_all[:, :, t:t + 3].contiguous(), v_all[:, :, t:t + 3].contiguous(),
+                               lg_all[:, :, t:t + 3].contiguous())
+            t += 3
+            continue
+        a.append(kk[t], vv[t], ll[t])
+        a.decode_attention(qq[t], out=out_a[t], scale=wl.scale)
+        if t % 41 == 0:  # the same token as a single append and a plain decode on b
+            b.append(kk[t], vv[t], ll[t])
+            b.decode_attention(qq[t], out=out_b[t], scale=wl.scale)
+        else:
+            b.step(kk[t], vv[t], ll[t], qq[t], out_b[t], scale=wl.scale)
+        t += 1
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    assert torch.equal(a.lengths(), b.lengths())
+    assert torch.equal(a.slot_positions(), b.slot_positions())
+    ka, va = a.export_kv()
+    kb, vb = b.export_kv()
+    assert torch.equal(ka, kb) and torch.equal(va, vb)
+    assert a.position == b.position == T
+    assert a.status() == b.status() == (dms.DMS_ERR_CAPACITY if logits[0] == "const" else dms.DMS_OK)
+    a.close()
+    b.close()
+
+
 def test_qwen3_8b_full_size_step_equals_append_then_decode():
     """The benchmark's timed step at full size (B32, Hq32/Hkv8, d128, n=16384,
     CR 8): 8 dms_step calls after a 16376-token history, against dms_append +
@@ -508,6 +566,69 @@ def test_step_graph_equals_dms_step_per_layer(shape):
     with pytest.raises(dms.DmsError):
         dms.DmsStepGraph([got[0], got[0]], kb[:2], vb[:2], lb[:2], qb[:2], ob[:2], wl.scale)
     for c in ref + got + [f]:
+        c.close()
+
+
+def test_step_graph_back_to_back_replays():
+    """A 4-layer step graph replayed for many tokens with no host
+    synchronisation: each token's inputs are copied into the bound buffers and
+    its outputs copied out on the stream, so layers after the first start
+    early under the previous layer.  Twice, every layer takes a chunk of two
+    tokens outside the graph, which makes the next launch run per layer.
+    Outputs and final state equal dms_step per layer, bit for bit."""
+    wl = _small("graph-b2b", 2, 8, 2, 128, 16, 400, ("normal", 0.6, 1.0), seed=23)
+    L, T0, T = 4, 24, 300
+    data = [tuple(x.cuda() for x in W.kv_range(wl, layer, 0, T)) + (W.q_range(wl, layer, 0, T).cuda(),)
+            for layer in range(L)]
+    ref = [dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w) for _ in range(L)]
+    got = [dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w) for _ in range(L)]
+    for layer in range(L):
+        k, v, lg, _ = data[layer]
+        for c in (ref[layer], got[layer]):
+            c.append_chunk(k[:, :, :T0].contiguous(), v[:, :, :T0].contiguous(), lg[:, :, :T0].contiguous())
+    kb = [torch.empty((wl.B, wl.Hkv, wl.D), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    vb = [torch.empty_like(x) for x in kb]
+    lb = [torch.empty((wl.B, wl.Hkv), dtype=torch.float32, device="cuda") for _ in range(L)]
+    qb = [torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    ob = [torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda") for _ in range(L)]
+    graph = dms.DmsStepGraph(got, kb, vb, lb, qb, ob, wl.scale)
+    hist_got = torch.zeros((T, L, wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    hist_ref = torch.zeros_like(hist_got)
+    t = T0
+    while t < T:
+        if t in (100, 201):
+            for layer in range(L):
+                k, v, lg, _ = data[layer]
+                for c in (ref[layer], got[layer]):
+                    c.append_chunk(k[:, :, t:t + 2].contiguous(), v[:, :, t:t + 2].contiguous(),
+                                   lg[:, :, t:t + 2].contiguous())
+            t += 2
+            continue
+        for layer in range(L):
+            k, v, lg, q = data[layer]
+            kb[layer].copy_(k[:, :, t])
+            vb[layer].copy_(v[:, :, t])
+            lb[layer].copy_(lg[:, :, t])
+            qb[layer].copy_(q[:, :, t])
+        graph.launch()
+        for layer in range(L):
+            hist_got[t, layer].copy_(ob[layer])
+            k, v, lg, q = data[layer]
+            ref[layer].step(k[:, :, t].contiguous(), v[:, :, t].contiguous(), lg[:, :, t].contiguous(),
+                            q[:, :, t].contiguous(), hist_ref[t, layer], scale=wl.scale)
+        t += 1
+    torch.cuda.synchronize()
+    assert torch.equal(hist_got, hist_ref)
+    for layer in range(L):
+        assert got[layer].position == ref[layer].position == T
+        assert torch.equal(got[layer].lengths(), ref[layer].lengths())
+        assert torch.equal(got[layer].slot_positions(), ref[layer].slot_positions())
+        ka, va = got[layer].export_kv()
+        kr, vr = ref[layer].export_kv()
+        assert torch.equal(ka, kr) and torch.equal(va, vr)
+        assert got[layer].status() == dms.DMS_OK
+    graph.close()
+    for c in ref + got:
         c.close()
 
 
