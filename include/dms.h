@@ -142,14 +142,26 @@ int dms_append_chunk(dms_cache_t* cache, const void* k, const void* v, const flo
  * carried as two bf16 terms, fp32 accumulation); then the chunk is appended
  * as by dms_append_chunk.  q_heads as for dms_decode_attention.  On an FP8
  * cache (dms_cache_create_ex) it runs the `chunk` rounds of dms_append +
- * dms_decode_attention themselves, token by token.
+ * dms_decode_attention themselves, token by token: per token a few pitched
+ * device-to-device copies gather its rows, then one append and one decode
+ * launch, then a copy scatters its output row (about six stream operations
+ * per token).  If one of them fails to enqueue, the call returns the error
+ * and the cache stays at the position of the last round that was enqueued in
+ * full (the tokens before it are appended, the rest are not).
  */
 int dms_prefill(dms_cache_t* cache, const void* q, const void* k, const void* v, const float* logits, int chunk,
                 float* out, float scale, int q_heads, void* stream);
 
 /*
  * Decode attention for the query of the last appended token, over every
- * retained slot of each (sequence, KV head):
+ * retained slot of each (sequence, KV head).  This is the step the method is
+ * built to make cheaper: autoregressive decoding reads the whole KV cache at
+ * every step, so its cost is the KV-cache token reads ("Inference-Time
+ * Hyper-Scaling with KV Cache Compression", notes page, section "研究背景与动机";
+ * AI research-map summary, "Experimental setup": KV-cache token reads), and
+ * DMS cuts them by evicting tokens after the delay window (same summary,
+ * "Approach").  The attention itself is plain softmax attention over the
+ * retained keys:
  *   q    bf16 [batch][q_heads][head_dim]
  *   out  fp32 [batch][q_heads][head_dim]
  *   out[b][g] = softmax(scale * K_h q_g) V_h over the retained keys of KV head
@@ -166,10 +178,21 @@ int dms_decode_attention(dms_cache_t* cache, const void* q, float* out, float sc
                          void* stream);
 
 /*
- * One decode step in one call: dms_append(k, v, evict_logit) followed by
- * dms_decode_attention(q, out, scale, q_heads), with the arguments checked once
- * -- the same two kernels on `stream`, for callers that issue a step per layer
- * per token and want one library crossing for it.
+ * One decode step in one call: the result of dms_append(k, v, evict_logit)
+ * followed by dms_decode_attention(q, out, scale, q_heads), bit for bit, with
+ * the arguments checked once (the method's decode step: append with delayed
+ * eviction, then attention over the retained cache; AI research-map summary,
+ * "Approach").
+ *  - bf16 caches: ONE kernel launch.  The decode kernel appends the token to
+ *    every head (into generations of the cache state that the launch does not
+ *    read) and attends over the cache after the append.  When the previous
+ *    call that advanced the cache added one token (dms_append, dms_step, or a
+ *    step-graph launch) and window >= 2, the launch computes its lengths and
+ *    work split and starts its first tile copies before the previous kernel
+ *    on the stream has finished (programmatic dependent launch); it reads its
+ *    inputs and writes anything only after that kernel has completed, so it
+ *    may follow any kernel that produces q, k, v or evict_logit.
+ *  - FP8 caches: two launches, the append kernel then the decode kernel.
  */
 int dms_step(dms_cache_t* cache, const void* k, const void* v, const float* evict_logit, const void* q, float* out,
              float scale, int q_heads, void* stream);
@@ -264,7 +287,13 @@ const char* dms_error_string(int code);
  *                   tokens of (b, h) in slots [0, len[b][h]).  V rows are in
  *                   plain element order.  K rows use the library's layout:
  *                   16-byte chunk c of slot s is stored at chunk c ^ (s & 7).
- *   len             int32 [batch][kv_heads], each >= 1 (device memory)
+ *   len             int32 [batch][kv_heads] (device memory): the retained
+ *                   length of each head, normally 1 .. capacity.  The kernel
+ *                   clamps every value to [0, capacity] before using it (a
+ *                   value outside that range can never send a read past a
+ *                   head's pool) and latches a length error in the scratch's
+ *                   error word; a head whose length is 0 after clamping has no
+ *                   keys, and its output rows are left unwritten.
  *   q, out, scale, q_heads: as for dms_decode_attention.
  * All pointers are device memory of the current device, 16-byte aligned
  * (len 4-byte aligned).

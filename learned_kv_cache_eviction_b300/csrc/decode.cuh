@@ -71,29 +71,33 @@ struct DecodeShape {
   static constexpr int QV = (G * D / 8 + 31) / 32;  // 16-byte q chunks per lane
   static constexpr int OFF_P = OFF_QS + ((G * QROW * 4 + 15) / 16) * 16;
   static constexpr int OFF_BAR = OFF_P + TK * PROW * 4;
-  // Fused step: per-warp state kept in shared memory rather than in registers
-  // (the decode loop has none to spare): the new token's slots of the first
-  // FX_HEADS heads of the warp's range, the first head, the current segment's,
-  // and the step's position.
-  static constexpr int FX_HEADS = 12;
-  static constexpr int FX_I0 = FX_HEADS, FX_SEG = FX_HEADS + 1;
-  static constexpr int FX_T = FX_HEADS + 2;  // the step's position t (int64, two slots)
+  // Per-warp state kept in shared memory rather than in registers (the decode
+  // loop has none to spare): the retained lengths of the first FX_HEADS heads
+  // of the warp's range (read at every head change, so no head change waits on
+  // global memory), and for the fused step the new token's slots of the same
+  // heads, the current segment's, and the step's position; then the first head.
+  static constexpr int FX_HEADS = 6;
+  static constexpr int FX_HL = 0, FX_SN = FX_HEADS;
+  static constexpr int FX_I0 = 2 * FX_HEADS, FX_SEG = 2 * FX_HEADS + 1;
+  static constexpr int FX_T = 2 * FX_HEADS + 2;  // the step's position t (int64, two slots)
   static constexpr int OFF_FX = OFF_BAR + NST * 8;
-  static constexpr int FX_BYTES = FP8 ? 0 : (FX_T + 2) * 4;  // through the int64 position; bf16 only
-  // Then an mbarrier for the bulk copies of a merge, the deferred arrival of
-  // the warp's first segment (see decode_kernel): {virtual head, index of its
-  // first partial, partial count, arrivals before this warp's}, and the merge
-  // mbarrier's phase.
+  static constexpr int FX_BYTES = (FX_T + 2) * 4;  // through the int64 position
+  // Then two mbarriers for the bulk copies of a merge, and the warp's split
+  // segments whose arrivals are counted once its range is done (see
+  // decode_kernel): {virtual head, index of its first partial, partial count}
+  // for the first and for the last segment (head -1: none), and the merge
+  // mbarriers' phase bits.
   static constexpr int OFF_MB = OFF_FX + FX_BYTES;
-  static constexpr int OFF_DEF = OFF_MB + 8;
-  static constexpr int WARP_BYTES = ((OFF_DEF + 20 + 127) / 128) * 128;
+  static constexpr int OFF_DEF = OFF_MB + 16;
+  static constexpr int WARP_BYTES = ((OFF_DEF + 28 + 127) / 128) * 128;
   // Partials: acc [G][D] floats, and (max, sum) of the G heads padded to a
   // 16-byte record of MLS floats, so that consecutive partials form one
-  // contiguous bulk copy.  A merge stages up to PM of them at a time in the
-  // warp's tile buffers, which are free once its range is done.
+  // contiguous bulk copy.  A merge stages them PM at a time in two halves of
+  // the warp's tile, q and probability buffers (free once its range is done),
+  // the copy of one chunk in flight while the other is folded in.
   static constexpr int MLS = (2 * G + 3) / 4 * 4;
-  static constexpr int STAGE_BYTES = NST * (TILEB_K + TILEB_V);
-  static constexpr int PM = STAGE_BYTES / (G * D * 4 + MLS * 4);
+  static constexpr int STAGE_HALF = (OFF_BAR / 2) / 16 * 16;
+  static constexpr int PM = STAGE_HALF / (G * D * 4 + MLS * 4);
   static constexpr int kSmemBudget = 227 * 1024 - 1024;  // leaves room for static shared memory
   // Warps per CTA: 12 (three per scheduler) where the shared memory allows.  With
   // three warps on a scheduler its register file leaves 168 registers per thread;
@@ -104,8 +108,8 @@ struct DecodeShape {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(G >= 1 && G <= 8, "1 <= G <= 8");
   static_assert(NW >= 4, "at least four warps per CTA");
-  static_assert(PM >= 1 && OFF_MB % 8 == 0, "merge staging");
-  static_assert(FP8 || (OFF_FX % 8 == 0 && OFF_FX + FX_T * 4 + 8 <= OFF_MB), "the position word lies inside FX");
+  static_assert(PM >= 1 && OFF_MB % 8 == 0 && STAGE_HALF % 16 == 0, "merge staging");
+  static_assert(OFF_FX % 8 == 0 && OFF_FX + FX_T * 4 + 8 <= OFF_MB, "the position word lies inside FX");
 };
 
 // Largest number of warps per CTA of any instantiation (sizes the partials).
@@ -113,10 +117,11 @@ constexpr int kMaxWarpsPerCta = 12;
 
 // Fewest tiles a warp is given (bounds the number of partials when the cache
 // is small).  Small caches are latency-bound per warp, so they are spread over
-// as many warps as this allows.  kMinSlotsPerWarp sizes the grid on the host
-// (two tiles of the 16-slot kernels).
-constexpr int kMinTilesPerWarp = 2;
-constexpr int kMinSlotsPerWarp = 32;
+// as many warps as this allows (three tiles measured best on small caches;
+// capping the warps per head instead, for fewer partials, was slower).
+// kMinSlotsPerWarp sizes the grid on the host.
+constexpr int kMinTilesPerWarp = 3;
+constexpr int kMinSlotsPerWarp = 48;
 
 struct DecodeArgs {
   const uint4* K;
@@ -166,7 +171,23 @@ struct DecodeArgs {
   // The host sets it only when the previous call that advanced the cache added
   // exactly one token (so generation t - 1 of the lengths is intact).
   int early;
+  // Work split: every warp gets at least min_tiles tiles.
+  int min_tiles;
+  // Plain decode over caller-owned lengths (the no-allocation entry point):
+  // each length is clamped to [0, cap] before use, and a clamped value latches
+  // kErrBitLength, so that a bad length can never send a copy past a head's pool.
+  int clamp_len;
 };
+
+// Length of head x in a plain decode, clamped when the lengths come from the caller.
+__device__ __forceinline__ int plain_len(const DecodeArgs& a, int x) {
+  int L = a.len[x];
+  if (a.clamp_len && static_cast<unsigned>(L) > static_cast<unsigned>(a.cap)) {
+    L = L < 0 ? 0 : a.cap;
+    atomicOr(a.err, kErrBitLength);
+  }
+  return L;
+}
 
 // The new token's slot in head x for the fused step at position t: the slot of
 // token t - w if that token was stored and marked (it leaves now), else the
@@ -246,7 +267,7 @@ __device__ __forceinline__ int decode_len(const DecodeArgs& a, int64_t t, int x)
     const bool retire = t >= a.w && a.ring_flag[ring_index(a.NH, a.w, x, t - a.w)] != 0;
     return (!retire && L < a.cap) ? L + 1 : L;
   }
-  return a.len[x];
+  return plain_len(a, x);
 }
 
 // Tiles of TK slots in a head of L retained slots (the last one partial).
@@ -345,35 +366,30 @@ __device__ __forceinline__ void scan_lengths(const LenF& len, int NH, int* pre) 
   __syncthreads();
 }
 
-// Arrival counts of split heads.  A warp writes its partial, synchronises
-// (__syncwarp), and lane 0 adds its arrival with release semantics at GPU
-// scope, which publishes the whole warp's partial; the arrival that completes
-// the count also acquires the others' partials.
-__device__ __forceinline__ int arrive_acq_rel(int32_t* cnt) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(cnt) : "memory");
-  return old;
-}
-__device__ __forceinline__ int arrive_release(int32_t* cnt) {
-  int old;
-  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(cnt) : "memory");
-  return old;
-}
+// Arrival counts of split heads.  A warp writes its partials, synchronises
+// (__syncwarp), and lane 0 issues a release fence at GPU scope, which publishes
+// the whole warp's partials, then adds its arrivals (relaxed, issued back to
+// back); an arrival that completes a count is followed by an acquire fence
+// before the others' partials are read.
+__device__ __forceinline__ void fence_release_gpu() { asm volatile("fence.release.gpu;" ::: "memory"); }
 __device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acquire.gpu;" ::: "memory"); }
+
 
 // Merge the nseg partials (max m, sum l, unnormalised acc) of one head, stored
 // at consecutive partial indices base, base + 1, ..., and write the normalised
 // output (outp already offset by lane * EL).  The partials are staged into
-// shared memory (`stage`, the warp's free tile buffers) by bulk copies of PM
-// partials at a time -- one round trip to L2 for a typical head -- and folded
-// in with a running max per query head.  The caller has acquired the partials
-// (fence after the arrival count); the proxy fence orders those generic-proxy
-// writes before the async-proxy reads of the bulk copy.  Returns false if a
-// copy did not complete within the time limit.
+// shared memory (`stage`: two halves of STAGE_HALF bytes, the warp's free
+// buffers) by bulk copies of PM partials at a time, chunk c + 1 in flight while
+// chunk c is folded in with a running max per query head.  The caller has
+// acquired the partials; the proxy fence orders those generic-proxy writes
+// before the async-proxy reads of the bulk copies.  `phases` holds the two
+// mbarriers' phase bits.  Returns false if a copy did not complete within the
+// time limit.
 template <typename Sh>
 __device__ __forceinline__ bool merge_partials(const DecodeArgs& a, size_t base, int nseg, float* outp, int lane,
-                                               uint8_t* stage, uint64_t* mbar, uint32_t& mphase) {
-  constexpr int G = Sh::G, D = Sh::D, EL = D / 32, MLS = Sh::MLS, PM = Sh::PM;
+                                               uint8_t* stage, uint64_t* mbar, uint32_t& phases) {
+  constexpr int G = Sh::G, D = Sh::D, EL = D / 32, MLS = Sh::MLS, PM = Sh::PM, HALF = Sh::STAGE_HALF;
+  constexpr int ACCB = G * D * 4;
   float M[G], L[G];
   float2 acc[G][EL / 2];
 #pragma unroll
@@ -383,22 +399,31 @@ __device__ __forceinline__ bool merge_partials(const DecodeArgs& a, size_t base,
 #pragma unroll
     for (int e = 0; e < EL / 2; ++e) acc[g][e] = make_float2(0.f, 0.f);
   }
-  if (lane == 0) asm volatile("fence.proxy.async;" ::: "memory");
-  const float* sacc = reinterpret_cast<const float*>(stage);
-  const float* sml = reinterpret_cast<const float*>(stage + PM * G * D * 4);
-  for (int k0 = 0; k0 < nseg; k0 += PM) {
-    const int n = min(PM, nseg - k0);
+  const int nch = (nseg + PM - 1) / PM;
+  auto issue = [&](int c) {
     if (lane == 0) {
-      const uint32_t ab = static_cast<uint32_t>(n * G * D * 4), mb = static_cast<uint32_t>(n * MLS * 4);
-      mbar_arrive_expect_tx(mbar, ab + mb);
-      bulk_copy_g2s(stage, a.part_acc + (base + k0) * G * D, ab, mbar);
-      bulk_copy_g2s(stage + PM * G * D * 4, a.part_ml + (base + k0) * MLS, mb, mbar);
+      const int b = c & 1, n = min(PM, nseg - c * PM);
+      uint8_t* dst = stage + b * HALF;
+      const uint32_t ab = static_cast<uint32_t>(n * ACCB), mb = static_cast<uint32_t>(n * MLS * 4);
+      mbar_arrive_expect_tx(&mbar[b], ab + mb);
+      bulk_copy_g2s(dst, a.part_acc + (base + static_cast<size_t>(c) * PM) * G * D, ab, &mbar[b]);
+      bulk_copy_g2s(dst + PM * ACCB, a.part_ml + (base + static_cast<size_t>(c) * PM) * MLS, mb, &mbar[b]);
     }
-    if (!mbar_wait(mbar, mphase)) {
-      (void)mbar_wait(mbar, mphase);  // give the copy in flight a second bounded wait before leaving
+  };
+  if (lane == 0) asm volatile("fence.proxy.async;" ::: "memory");
+  issue(0);
+  if (nch > 1) issue(1);
+  for (int c = 0; c < nch; ++c) {
+    const int b = c & 1, n = min(PM, nseg - c * PM);
+    const uint32_t ph = (phases >> b) & 1u;
+    if (!mbar_wait(&mbar[b], ph)) {
+      // give the copies in flight a second bounded wait before leaving
+      for (int k = c; k < min(nch, c + 2); ++k) (void)mbar_wait(&mbar[k & 1], (phases >> (k & 1)) & 1u);
       return false;
     }
-    mphase ^= 1u;
+    phases ^= 1u << b;
+    const float* sacc = reinterpret_cast<const float*>(stage + b * HALF);
+    const float* sml = reinterpret_cast<const float*>(stage + b * HALF + PM * ACCB);
     float mt[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) mt[g] = M[g];
@@ -432,6 +457,7 @@ __device__ __forceinline__ bool merge_partials(const DecodeArgs& a, size_t base,
       }
     }
     __syncwarp();
+    if (c + 2 < nch) issue(c + 2);  // this half has been read
   }
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -478,9 +504,9 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   auto real_head = [&](int v) { return v >= a.NH ? v - a.NH : v; };
   auto head_group = [&](int v) { return v >= a.NH ? 1 : 0; };
   int* pre = reinterpret_cast<int*>(smem);  // [NV + 1]; aliases the warp regions until the barrier below
-  int* sn = pre + NV + 1;                   // fused step: [NH] the new token's slot in each KV head
+  int* ln = pre + NV + 1;                   // [NH] each KV head's retained length (fused: after the append)
+  int* sn = ln + a.NH;                      // fused step: [NH] the new token's slot in each KV head
   int* sp = sn + a.NH;                      // fused step started early: [NH] the previous token's slot
-  int* ln = sp + a.NH;                      // fused step: [NH] each KV head's length after the append
   // Fused step: warp x of the grid appends the token to head x (and x + nwarps,
   // ...).  Its row chunk (K for lanes < CH, V for lanes CH .. 2 CH - 1) and
   // logit are loaded now, in flight during the scan (not when started early:
@@ -523,7 +549,9 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
       }
       return tiles_of<TK>(L3);
     } else {
-      return tiles_of<TK>(a.len[x]);
+      const int L = plain_len(a, x);
+      if (v < a.NH) ln[x] = L;
+      return tiles_of<TK>(L);
     }
   };
   scan_lengths(scanf, NV, pre);
@@ -564,7 +592,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   }
   const int64_t S = pre[NV];  // tiles of all heads
   int64_t Pe = nwarps;
-  if (S / kMinTilesPerWarp < Pe) Pe = S / kMinTilesPerWarp;
+  if (S / a.min_tiles < Pe) Pe = S / a.min_tiles;
   if (Pe < 1) Pe = 1;
   const bool active = S > 0 && wg < Pe;
   int64_t A = 0, E = 0, P0 = 0;
@@ -584,7 +612,8 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   // barrier, which ends the prefix sums' lease on the warp regions).  Started
   // early: also the slot of the previous step's token in head i0 (its tile is
   // not copied before the wait), and this warp's own head to append.
-  int snl = -1, sprev0 = -1, own_sn = -1, own_L = 0;
+  int snl = -1, hll = 0, sprev0 = -1, own_sn = -1, own_L = 0;
+  if (active && lane < Sh::FX_HEADS && i0 + lane < NV) hll = ln[real_head(i0 + lane)];
   if constexpr (FUSED) {
     if (active && lane < Sh::FX_HEADS && i0 + lane < NV) snl = sn[real_head(i0 + lane)];
     if (early) {
@@ -607,29 +636,35 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   float* pb = reinterpret_cast<float*>(wbase + Sh::OFF_P);
   uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + Sh::OFF_BAR);  // [NST] tiles
   int* fx = reinterpret_cast<int*>(wbase + Sh::OFF_FX);               // fused-step state
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(wbase + Sh::OFF_MB);   // merge copies
-  int* def = reinterpret_cast<int*>(wbase + Sh::OFF_DEF);              // deferred arrival, merge phase
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(wbase + Sh::OFF_MB);   // [2] merge copies
+  int* def = reinterpret_cast<int*>(wbase + Sh::OFF_DEF);              // split segments, merge phases
   if (active) {
     if (lane == 0) {
       for (int x = 0; x < NST; ++x) mbar_init(&bars[x], 1);
-      mbar_init(mbar, 1);
+      mbar_init(&mbar[0], 1);
+      mbar_init(&mbar[1], 1);
       fence_barrier_init();
       def[0] = -1;
-      def[4] = 0;
+      def[3] = -1;
+      def[6] = 0;
     }
+    if (lane < Sh::FX_HEADS) fx[Sh::FX_HL + lane] = hll;
+    if (lane == 0) fx[Sh::FX_I0] = i0;
     if constexpr (FUSED) {
-      if (lane < Sh::FX_HEADS) fx[lane] = snl;
+      if (lane < Sh::FX_HEADS) fx[Sh::FX_SN + lane] = snl;
       if (lane == 0) {
-        fx[Sh::FX_I0] = i0;
         fx[Sh::FX_SEG] = -1;
         *reinterpret_cast<int64_t*>(fx + Sh::FX_T) = t_step;
       }
     }
   }
   __syncwarp();
-  // Retained length of head x after this launch's append (read per head
-  // change; the position comes from shared memory, not a register).
+  // Retained length of virtual head v as this launch decodes it (fused: after
+  // its append), read per head change: from the warp's cached lengths, else
+  // from global memory (the position comes from shared memory, not a register).
   auto lenf = [&](int v) {
+    const int d = v - fx[Sh::FX_I0];
+    if (static_cast<unsigned>(d) < static_cast<unsigned>(Sh::FX_HEADS)) return fx[Sh::FX_HL + d];
     if constexpr (FUSED) return decode_len<true>(a, *reinterpret_cast<const int64_t*>(fx + Sh::FX_T), real_head(v));
     else return decode_len<false>(a, 0, real_head(v));
   };
@@ -722,21 +757,16 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
     const int x = real_head(v);
     const int b = x / a.Hkv, h = x - b * a.Hkv;
     float* outp = a.out + (static_cast<size_t>(b) * Hq + h * a.Gq + head_group(v) * G) * D + lane * EL;
-    uint32_t ph = static_cast<uint32_t>(def[4]);
+    uint32_t ph = static_cast<uint32_t>(def[6]);
     const bool ok = merge_partials<Sh>(a, base, nseg, outp, lane, wbase, mbar, ph);
     __syncwarp();
     if (lane == 0) {
-      def[4] = static_cast<int>(ph);
+      def[6] = static_cast<int>(ph);
       a.head_cnt[v] = 0;  // for the next call
       if (!ok) atomicOr(a.err, kErrBitTimeout);
     }
     __syncwarp();
   };
-  // The arrival count of the warp's first segment when later segments follow
-  // (lane 0; -1 when none is pending).  It is read only after the next tile has
-  // landed, so the stream never waits on it.
-  int pend = -1;
-
   // QK lane roles: two lanes per slot, each over half of the head dim.
   const int r = lane & 15, hf = lane >> 4;
   float m[G], l[G];
@@ -778,7 +808,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
       if constexpr (FUSED) {
         const int d = cs.i - fx[Sh::FX_I0];
         const int sw =
-            d < Sh::FX_HEADS ? fx[d]
+            d < Sh::FX_HEADS ? fx[Sh::FX_SN + d]
                              : fused_new_slot_far(a, *reinterpret_cast<const int64_t*>(fx + Sh::FX_T), real_head(cs.i));
         __syncwarp();
         if (lane == 0) fx[Sh::FX_SEG] = sw;
@@ -793,10 +823,6 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
     if (n_issued <= n_cons || !mbar_wait(&bars[buf], (n_cons / NST) & 1)) {
       fail_and_drain();
       return;
-    }
-    if (pend >= 0) {
-      def[3] = pend;
-      pend = -1;
     }
 
     if constexpr (FUSED) {
@@ -1058,36 +1084,36 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
           }
           reinterpret_cast<float2*>(a.part_ml + idx * Sh::MLS)[lane] = make_float2(mm, ll);
         }
-        // Release the partial, then count this arrival; the last of the head's
-        // nseg warps merges (acquire) and resets the counter.  Only a warp's first
-        // segment can be split and followed by more: its count is looked at once
-        // the range is done (the other pieces of that head end their warps'
-        // ranges, so it is rarely the last), and the stream goes on meanwhile.
-        const int nseg = static_cast<int>(w1 - w0) + 1;
-        __syncwarp();
-        if (cs.valid) {
-          if (lane == 0) {
-            def[0] = seg_i;
-            def[1] = static_cast<int>(w0 + seg_i);
-            def[2] = nseg;
-            pend = arrive_release(a.head_cnt + seg_i);
-          }
-        } else {
-          int last = 0;
-          if (lane == 0) last = arrive_acq_rel(a.head_cnt + seg_i) == nseg - 1;
-          last = __shfl_sync(0xffffffffu, last, 0);
-          if (last) merge_head(seg_i, static_cast<size_t>(w0 + seg_i), nseg);
+        // The arrival is counted once the warp's range is done (below): only a
+        // warp's first and last segments can be split, and the other pieces of a
+        // head end their warps' ranges too, so the stream never waits on a count.
+        if (lane == 0) {
+          const int k = cs.valid ? 0 : 3;
+          def[k] = seg_i;
+          def[k + 1] = static_cast<int>(w0 + seg_i);
+          def[k + 2] = static_cast<int>(w1 - w0) + 1;
         }
       }
     }
     try_issue();
   }
-  // The deferred first segment: merge it if this warp's arrival was the last.
-  if (pend >= 0) def[3] = pend;
+  // Count the arrivals of the warp's split segments (release the partials
+  // first); the last of a head's nseg warps merges (acquire) and resets its
+  // counter.
   __syncwarp();
-  if (def[0] >= 0 && def[3] == def[2] - 1) {
-    if (lane == 0) fence_acquire_gpu();
-    merge_head(def[0], static_cast<size_t>(def[1]), def[2]);
+  const int v0 = def[0], v1 = def[3];
+  if (v0 >= 0 || v1 >= 0) {
+    int last = 0;
+    if (lane == 0) {
+      fence_release_gpu();
+      const int c0 = v0 >= 0 ? atomicAdd(a.head_cnt + v0, 1) : -1;
+      const int c1 = v1 >= 0 ? atomicAdd(a.head_cnt + v1, 1) : -1;
+      last = (v0 >= 0 && c0 == def[2] - 1 ? 1 : 0) | (v1 >= 0 && c1 == def[5] - 1 ? 2 : 0);
+      if (last) fence_acquire_gpu();
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last & 2) merge_head(v1, static_cast<size_t>(def[4]), def[5]);
+    if (last & 1) merge_head(v0, static_cast<size_t>(def[1]), def[2]);
   }
 }
 

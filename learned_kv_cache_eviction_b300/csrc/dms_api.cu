@@ -4,6 +4,7 @@
 // at creation time and launches.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -137,7 +138,7 @@ bool step_can_start_early(const dms_cache* c) { return c->w >= 2 && c->t >= 1 &&
 template <int D, int G, bool FUSED, int KVF>
 int decode_attr(const dms_cache* c) {
   using Sh = dms::DecodeShape<D, G, KVF>;
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64] = {};  // set once per device; threads may race to set it
   if (c->device < 64 && attr_done[c->device]) return DMS_OK;
   if (cudaFuncSetAttribute(dms::decode_kernel<D, G, FUSED, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Sh::SMEM) != cudaSuccess) {
@@ -156,8 +157,8 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
   using Sh = dms::DecodeShape<D, G, KVF>;
   if (decode_attr<D, G, FUSED, KVF>(c) != DMS_OK) return DMS_ERR_CUDA;
   const int64_t NV = static_cast<int64_t>(c->NH) * nsplit;
-  // The prologue's prefix sums (and, fused, each head's new and previous slot and length) fit in shared memory.
-  if ((NV + 1 + (FUSED ? 3 * c->NH : 0)) * 4 > Sh::SMEM) return DMS_ERR_INVALID_ARG;
+  // The prologue's prefix sums and lengths (and, fused, each head's new and previous slot) fit in shared memory.
+  if ((NV + 1 + c->NH + (FUSED ? 2 * c->NH : 0)) * 4 > Sh::SMEM) return DMS_ERR_INVALID_ARG;
   // Upper bound of the retained slots (the exact sum lives on the device); a
   // graph-replayed step runs at positions unknown now, so it takes the capacity.
   const bool graph = FUSED && in != nullptr && in->t_dev != nullptr;
@@ -194,6 +195,8 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
   a.t = c->t;
   a.w = c->w;
   a.early = 0;
+  a.min_tiles = dms::kMinTilesPerWarp;
+  a.clamp_len = 0;
   if constexpr (FUSED) {
     a.k_new = in->k;
     a.v_new = in->v;
@@ -231,7 +234,7 @@ int launch_decode_d(dms_cache* c, const void* q, float* out, float scale, int G,
 template <int D, int G>
 int launch_prefill_t(dms_cache* c, const dms::PrefillArgs& a, cudaStream_t st) {
   using Sh = dms::PrefillShape<D, G>;
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64] = {};  // set once per device; threads may race to set it
   if (c->device < 64 && !attr_done[c->device]) {
     int optin = 0;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device) != cudaSuccess ||

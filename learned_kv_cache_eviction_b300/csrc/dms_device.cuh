@@ -11,6 +11,7 @@ namespace dms {
 // Sticky device error bits (the host maps them to DMS_ERR_* codes).
 constexpr int kErrBitCapacity = 1;
 constexpr int kErrBitTimeout = 2;
+constexpr int kErrBitLength = 4;  // a caller-supplied length outside [0, capacity] was clamped
 
 // Time limit of every device-side wait on an mbarrier (ns of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;

@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -33,7 +34,7 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 void* g_scratch_addr[kMaxDevices] = {};  // device address of g_scratch, per device
-bool g_attr_done[kMaxDevices][2][DMS_MAX_GROUP + 1] = {};
+std::atomic<bool> g_attr_done[kMaxDevices][2][DMS_MAX_GROUP + 1] = {};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -92,7 +93,7 @@ template <int D, int G>
 int run(int dev, int num_sms, unsigned char* scratch, const void* k_pool, const void* v_pool, const int32_t* len,
         int NH, int kv_heads, int capacity, const void* q, float* out, float scale, cudaStream_t st) {
   using Sh = dms::DecodeShape<D, G>;
-  if (static_cast<int64_t>(NH + 1) * 4 > Sh::SMEM) return DMS_ERR_SCRATCH_LIMIT;
+  if ((2 * static_cast<int64_t>(NH) + 1) * 4 > Sh::SMEM) return DMS_ERR_SCRATCH_LIMIT;  // prologue prefix sums, lengths
   // Upper bound of the retained slots: every slot of every head.
   const int64_t smax = static_cast<int64_t>(NH) * capacity;
   const int64_t per_cta = int64_t(dms::kMinSlotsPerWarp) * Sh::NW;
@@ -128,6 +129,8 @@ int run(int dev, int num_sms, unsigned char* scratch, const void* k_pool, const 
   a.qscale = scale * 1.4426950408889634f;  // log2(e)
   a.Gq = G;
   a.nsplit = 1;
+  a.min_tiles = dms::kMinTilesPerWarp;
+  a.clamp_len = 1;  // the lengths are the caller's: never trust them to stay within the pools
   // The merge in the decode kernel needs every head counter at zero.  Calls that
   // complete leave them at zero; clearing them here (stream-ordered, no
   // allocation) also recovers from a call that stopped early.

@@ -331,6 +331,46 @@ def dms_decode_attention(cache: DmsCache, q, out=None, scale=None, stream=None):
     return cache.decode_attention(q, out, scale, stream)
 
 
+def dms_step(cache: DmsCache, k, v, evict_logit, q, out, scale=None, stream=None):
+    return cache.step(k, v, evict_logit, q, out, scale, stream)
+
+
+def dms_step_graph_create(caches, k, v, evict_logit, q, out, scale) -> DmsStepGraph:
+    return DmsStepGraph(caches, k, v, evict_logit, q, out, scale)
+
+
+def dms_step_graph_launch(graph: DmsStepGraph, stream=None) -> None:
+    graph.launch(stream)
+
+
+def dms_step_graph_destroy(graph: DmsStepGraph) -> None:
+    graph.close()
+
+
+def dms_decode_attention_noalloc(k_pool: torch.Tensor, v_pool: torch.Tensor, lengths: torch.Tensor, q: torch.Tensor,
+                                 out: torch.Tensor, scale: float | None = None, stream=None) -> torch.Tensor:
+    """Decode attention over caller-owned pools with no device allocation
+    (dms_decode_attention_noalloc).  k_pool, v_pool bf16 [B][Hkv][cap][D] (K in
+    the library's chunk-permuted row layout), lengths int32 [B][Hkv], q bf16
+    [B][Hq][D], out fp32 [B][Hq][D] (preallocated)."""
+    lib = load_library()
+    if k_pool.dim() != 4:
+        raise ValueError("k_pool must be [batch][kv_heads][capacity][head_dim]")
+    B, H, cap, D = k_pool.shape
+    dev = k_pool.device
+    Hq = q.shape[1] if q.dim() == 3 else -1
+    _need(k_pool, "k_pool", torch.bfloat16, (B, H, cap, D), dev)
+    _need(v_pool, "v_pool", torch.bfloat16, (B, H, cap, D), dev)
+    _need(lengths, "lengths", torch.int32, (B, H), dev)
+    _need(q, "q", torch.bfloat16, (B, Hq, D), dev)
+    _need(out, "out", torch.float32, (B, Hq, D), dev)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(lib.dms_decode_attention_noalloc(k_pool.data_ptr(), v_pool.data_ptr(), lengths.data_ptr(), B, H, cap, D,
+                                            q.data_ptr(), out.data_ptr(), scale, Hq, _stream_handle(stream)),
+           "dms_decode_attention_noalloc")
+    return out
+
+
 def dms_cache_lengths(cache: DmsCache, stream=None):
     return cache.lengths(stream)
 

@@ -323,20 +323,91 @@ def test_qwen3_8b_full_size_cr8_and_cr1():
         torch.cuda.empty_cache()
 
 
-def test_qwen_r1_width_sampled():
-    """Qwen-R1-32B-like width scaling (B64, G=5, per-head eviction 50-97%):
-    a 4096-token history, rows {0, 63}."""
+def test_qwen_r1_width_full_size():
+    """Qwen-R1-32B-like width scaling at its stated size: B64, Hq40/Hkv8 (G=5),
+    per-head eviction 50-97 %, 16380-token history filled in chunks, then 4
+    dms_step calls to 16384 tokens (the benchmark's launch configuration).
+    Bookkeeping of all 64 rows bit-exact after every step and the slot map at
+    the end; outputs of rows {0, 63} at every step against the oracle."""
     wl = W.WORKLOADS["qwen-r1-32b"].with_(chunk=512)
-    tr, _ = _prefill_then_decode(wl, 4092, 4, rows=[0, wl.B - 1])
+    rows = [0, wl.B - 1]
+    T0, T = wl.cap - 4, wl.cap
+    tr = Trajectory(wl, T, rows=rows)
+    while tr.t < T0:
+        tr.append_chunk(min(wl.chunk, T0 - tr.t))
+    tr.check_lengths()
+    q_all = W.q_range(wl, 0, T0, T)
+    out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    for t in range(T0, T):
+        q = q_all[:, :, t - T0].contiguous()
+        tr.cache.step(tr.k[:, :, t].contiguous().cuda(), tr.v[:, :, t].contiguous().cuda(),
+                      tr.lg[:, :, t].contiguous().cuda(), q.cuda(), out, scale=wl.scale)
+        tr.sim.append(tr.e[:, :, t])
+        tr.t += 1
+        tr.check_lengths()
+        ref = O.decode_attention(q[rows].float().numpy(), tr.k_np, tr.v_np, tr.e[rows], t, wl.w, wl.scale)
+        assert_attention_close(out.cpu().numpy()[rows], ref, f"qwen-r1-32b t={t}")
+    assert tr.cache.status() == dms.DMS_OK
+    tr.check_slots()
     lens = tr.sim.len
     assert lens.max() > 3 * lens.min()  # strongly imbalanced heads
+    assert 6.0 < T / lens.mean() < 10.0
+    tr.cache.close()
+    del tr
+    torch.cuda.empty_cache()
 
 
-def test_long_context_one_layer():
-    """Long-context stack, one of its 8 layers (B4, Hq64/Hkv8, d128): 32768-token
-    chunked fill + 4 decode steps, all rows."""
+def test_long_context_layer_prefill_and_4k_decode():
+    """One layer of the long-context stack as its workload states it: B4,
+    Hq64/Hkv8 (G=8), a 32768-token chunked prefill through dms_prefill (C=512;
+    outputs of rows {0, 3} checked at 3 positions of every 8th chunk), then
+    4096 decode steps through dms_step to 36864 tokens.  Lengths of all rows
+    bit-exact after every chunk and every step, the slot map at the end;
+    outputs of rows {0, 3} every 1024th step and at the last step."""
     wl = W.WORKLOADS["long-context"]
-    _prefill_then_decode(wl, wl.prefill, 4, rows=list(range(wl.B)), layer=3)
+    layer = 3
+    rows = [0, wl.B - 1]
+    T0, T = wl.prefill, wl.prefill + wl.decode
+    tr = Trajectory(wl, T, layer=layer, rows=rows)
+    n_chunk = 0
+    while tr.t < T0:
+        n = min(wl.chunk, T0 - tr.t)
+        t0 = tr.t
+        qc = W.q_range(wl, layer, t0, t0 + n)
+        sl = slice(t0, t0 + n)
+        out = tr.cache.prefill(qc.cuda(), tr.k[:, :, sl].contiguous().cuda(), tr.v[:, :, sl].contiguous().cuda(),
+                               tr.lg[:, :, sl].contiguous().cuda(), scale=wl.scale)
+        tr.sim.append_chunk(tr.e[:, :, sl])
+        tr.t += n
+        tr.check_lengths()
+        if n_chunk % 8 == 7:
+            got = out.cpu().numpy()[rows]
+            for c in (0, n // 2, n - 1):
+                ref = O.decode_attention(qc[rows][:, :, c].float().numpy(), tr.k_np, tr.v_np, tr.e[rows], t0 + c,
+                                         wl.w, wl.scale)
+                assert_attention_close(got[:, :, c], ref, f"long-context prefill position {t0 + c}")
+        n_chunk += 1
+    q_all = W.q_range(wl, layer, T0, T)
+    out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    n_checked = 0
+    for t in range(T0, T):
+        q = q_all[:, :, t - T0].contiguous()
+        tr.cache.step(tr.k[:, :, t].contiguous().cuda(), tr.v[:, :, t].contiguous().cuda(),
+                      tr.lg[:, :, t].contiguous().cuda(), q.cuda(), out, scale=wl.scale)
+        tr.sim.append(tr.e[:, :, t])
+        tr.t += 1
+        tr.check_lengths()
+        if (t + 1 - T0) % 1024 == 0 or t == T - 1:
+            ref = O.decode_attention(q[rows].float().numpy(), tr.k_np, tr.v_np, tr.e[rows], t, wl.w, wl.scale)
+            assert_attention_close(out.cpu().numpy()[rows], ref, f"long-context decode t={t}")
+            n_checked += 1
+    assert n_checked == 4
+    assert tr.cache.status() == dms.DMS_OK
+    tr.check_slots()
+    assert 6.5 < T / tr.sim.len.mean() < 9.5
+    tr.cache.close()
+    del tr
+    torch.cuda.empty_cache()
 
 
 def test_device_wait_time_limit_is_reported():
@@ -630,6 +701,60 @@ def test_step_graph_back_to_back_replays():
     graph.close()
     for c in ref + got:
         c.close()
+
+
+def test_step_graph_long_context_shape():
+    """The 8-layer step graph at the long-context stack's shapes (B4, Hq64/Hkv8,
+    d128, capacity 36864), every layer filled to 32768 tokens in chunks, then
+    16 token steps replayed from the graph with no host synchronisation
+    between them; outputs, lengths and slot maps equal dms_step on every
+    layer's twin cache, bit for bit."""
+    wl = W.WORKLOADS["long-context"]
+    L, T0, n = wl.layers, wl.prefill, 16
+    ref = [dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w) for _ in range(L)]
+    got = [dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w) for _ in range(L)]
+    for layer in range(L):
+        for t0 in range(0, T0, wl.chunk):
+            k, v, lg = W.kv_range(wl, layer, t0, t0 + wl.chunk, device="cuda")
+            ref[layer].append_chunk(k, v, lg)
+            got[layer].append_chunk(k, v, lg)
+    data = []
+    for layer in range(L):
+        k, v, lg = W.kv_range(wl, layer, T0, T0 + n, device="cuda")
+        q = W.q_range(wl, layer, T0, T0 + n, device="cuda")
+        data.append((k, v, lg, q))
+    kb = [torch.empty((wl.B, wl.Hkv, wl.D), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    vb = [torch.empty_like(x) for x in kb]
+    lb = [torch.empty((wl.B, wl.Hkv), dtype=torch.float32, device="cuda") for _ in range(L)]
+    qb = [torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    ob = [torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda") for _ in range(L)]
+    graph = dms.DmsStepGraph(got, kb, vb, lb, qb, ob, wl.scale)
+    hist_got = torch.zeros((n, L, wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    hist_ref = torch.zeros_like(hist_got)
+    for j in range(n):
+        for layer in range(L):
+            k, v, lg, q = data[layer]
+            kb[layer].copy_(k[:, :, j])
+            vb[layer].copy_(v[:, :, j])
+            lb[layer].copy_(lg[:, :, j])
+            qb[layer].copy_(q[:, :, j])
+        graph.launch()
+        for layer in range(L):
+            hist_got[j, layer].copy_(ob[layer])
+            k, v, lg, q = data[layer]
+            ref[layer].step(k[:, :, j].contiguous(), v[:, :, j].contiguous(), lg[:, :, j].contiguous(),
+                            q[:, :, j].contiguous(), hist_ref[j, layer], scale=wl.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(hist_got, hist_ref)
+    for layer in range(L):
+        assert got[layer].position == ref[layer].position == T0 + n
+        assert torch.equal(got[layer].lengths(), ref[layer].lengths())
+        assert torch.equal(got[layer].slot_positions(), ref[layer].slot_positions())
+        assert got[layer].status() == ref[layer].status() == dms.DMS_OK
+    graph.close()
+    for c in ref + got:
+        c.close()
+    torch.cuda.empty_cache()
 
 
 def test_qwen3_8b_decode_trajectory_1k_to_16k():

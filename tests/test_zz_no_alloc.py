@@ -90,3 +90,43 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     host = np.zeros(64, dtype=np.float32)
     assert lib.dms_decode_attention_noalloc(host.ctypes.data, p, p, 1, 8, 16, 128, p, p, 0.1, 32, s) == \
         dms.DMS_ERR_INVALID_ARG
+
+
+def test_noalloc_full_heads_and_clamped_lengths():
+    """Heads filled exactly to capacity (len == capacity) decode like
+    dms_decode_attention.  Lengths outside [0, capacity] come from the caller
+    and are clamped: a length above the capacity reads the full pool, a
+    negative one reads nothing and leaves that head's output rows unwritten."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    lib = dms.load_library()
+    B, Hq, Hkv, D, cap = 2, 8, 2, 128, 300
+    wl = W.Workload("noalloc-full", B=B, Hq=Hq, Hkv=Hkv, D=D, w=16, cap=cap, seed=23, logits=("const", -10.0))
+    k, v, lg = W.kv_range(wl, 0, 0, cap)
+    q = W.q_range(wl, 0, cap - 1, cap)[:, :, 0].contiguous().cuda()
+    cache = dms.DmsCache(B, Hkv, cap, D, wl.w)
+    cache.append_chunk(k.contiguous().cuda(), v.contiguous().cuda(), lg.contiguous().cuda())
+    lens = cache.lengths()
+    assert bool((lens == cap).all())
+    ref = cache.decode_attention(q, scale=wl.scale)
+    k_log, v_log = cache.export_kv()
+    k_pool, v_pool = _library_k_layout(k_log), v_log.contiguous()
+    stream = torch.cuda.current_stream().cuda_stream
+    G = Hq // Hkv
+    for bad in (False, True):
+        ln = lens.clone()
+        if bad:
+            ln[0, 0] = cap + 5    # clamped to cap: same as the full head
+            ln[1, 1] = -3         # clamped to 0: no keys, rows left as they were
+        out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+        rc = lib.dms_decode_attention_noalloc(k_pool.data_ptr(), v_pool.data_ptr(), ln.data_ptr(), B, Hkv, cap, D,
+                                              q.data_ptr(), out.data_ptr(), ctypes.c_float(wl.scale), Hq, stream)
+        assert rc == dms.DMS_OK, lib.dms_error_string(rc)
+        torch.cuda.synchronize()
+        keep = torch.ones((B, Hq), dtype=torch.bool, device="cuda")
+        if bad:
+            keep[1, G:2 * G] = False
+            assert bool(torch.isnan(out[1, G:2 * G]).all())
+        mx, rel = _close(out[keep], ref[keep])
+        assert mx <= TOL_MAX_ABS and rel <= TOL_MEAN_REL, (bad, mx, rel)
+    cache.close()
