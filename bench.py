@@ -640,8 +640,8 @@ def decode_bytes_fp8(wl, len_sum):
 def time_fp8_leg(dms, W, wl, device, steps):
     """FP8 (E4M3) storage at the headline shapes: the cache is filled to
     16384 - steps tokens, then `steps` timed dms_step calls (append + decode,
-    two launches for FP8 storage) and `steps` back-to-back dms_decode_attention
-    calls, with events around each pass."""
+    one fused launch, as for bf16 storage) and `steps` back-to-back
+    dms_decode_attention calls, with events around each pass."""
     lib = dms.load_library()
     stream = torch.cuda.current_stream(device)
     n0 = wl.cap - steps - 3
@@ -686,7 +686,7 @@ def time_fp8_leg(dms, W, wl, device, steps):
             "decode_us_per_launch_back_to_back": dec_us, "algorithmic_bytes_per_launch": alg,
             "achieved_GBps": alg / (dec_us * 1e-6) / 1e9,
             "kv_token_reads_per_step": 0.5 * (len0 + len1),
-            "note": "step = append kernel + decode kernel (the fused one-launch step is bf16 only)"}
+            "note": "step = one fused launch (the token is quantized and appended, then attended over)"}
 
 
 def time_graph_leg(dms, W, device, steps):

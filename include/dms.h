@@ -83,11 +83,11 @@ dms_cache_t* dms_cache_create(int batch, int kv_heads, int capacity, int head_di
  * K rows of head_dim + 16 bytes (codes, then {K scale, V scale} and 8 bytes of
  * padding), V rows of head_dim bytes, i.e. 2 * head_dim + 16 bytes per slot
  * against 4 * head_dim for bf16.  On an FP8 cache dms_prefill runs its
- * definition, `chunk` rounds of append + decode (one decode launch per token,
- * exact, far slower than the tensor-core path of bf16 caches), and dms_step
- * runs as two launches (append, then decode).  An FP8 cache also holds a
- * buffer for one token's rows of those rounds.  dms_decode_attention_noalloc
- * reads bf16 pools only.
+ * definition, `chunk` rounds of append + decode (one fused step launch per
+ * token, exact, far slower than the tensor-core path of bf16 caches); dms_step
+ * is one launch as on bf16 caches.  An FP8 cache also holds a buffer for one
+ * token's rows of those rounds.  dms_decode_attention_noalloc reads bf16 pools
+ * only.
  */
 dms_cache_t* dms_cache_create_ex(int batch, int kv_heads, int capacity, int head_dim, int window, int kv_format);
 
@@ -143,9 +143,9 @@ int dms_append_chunk(dms_cache_t* cache, const void* k, const void* v, const flo
  * as by dms_append_chunk.  q_heads as for dms_decode_attention.  On an FP8
  * cache (dms_cache_create_ex) it runs the `chunk` rounds of dms_append +
  * dms_decode_attention themselves, token by token: per token a few pitched
- * device-to-device copies gather its rows, then one append and one decode
- * launch, then a copy scatters its output row (about six stream operations
- * per token).  If one of them fails to enqueue, the call returns the error
+ * device-to-device copies gather its rows, then one launch of the fused step
+ * kernel (append + decode), then a copy scatters its output row (six stream
+ * operations per token).  If one of them fails to enqueue, the call returns the error
  * and the cache stays at the position of the last round that was enqueued in
  * full (the tokens before it are appended, the rest are not).
  */
@@ -183,16 +183,16 @@ int dms_decode_attention(dms_cache_t* cache, const void* q, float* out, float sc
  * the arguments checked once (the method's decode step: append with delayed
  * eviction, then attention over the retained cache; AI research-map summary,
  * "Approach").
- *  - bf16 caches: ONE kernel launch.  The decode kernel appends the token to
- *    every head (into generations of the cache state that the launch does not
- *    read) and attends over the cache after the append.  When the previous
+ *  - ONE kernel launch (bf16 or FP8 storage).  The decode kernel appends the
+ *    token to every head (into generations of the cache state that the launch
+ *    does not read; an FP8 cache quantizes it as dms_append does) and attends
+ *    over the cache after the append.  When the previous
  *    call that advanced the cache added one token (dms_append, dms_step, or a
  *    step-graph launch) and window >= 2, the launch computes its lengths and
  *    work split and starts its first tile copies before the previous kernel
  *    on the stream has finished (programmatic dependent launch); it reads its
  *    inputs and writes anything only after that kernel has completed, so it
  *    may follow any kernel that produces q, k, v or evict_logit.
- *  - FP8 caches: two launches, the append kernel then the decode kernel.
  */
 int dms_step(dms_cache_t* cache, const void* k, const void* v, const float* evict_logit, const void* q, float* out,
              float scale, int q_heads, void* stream);
@@ -240,8 +240,8 @@ int dms_cache_selftest_wait(dms_cache_t* cache, void* stream);
  * given scale and q_heads; then one node that advances every cache's
  * position.  The buffers are bound by address: before each launch the caller
  * writes that step's inputs into them, and after it reads out[i].  The caches
- * must be distinct bf16 caches on one device; the graph does not own them and
- * must be destroyed before they are.  Returns NULL on failure (dms_last_error()
+ * must be distinct caches (bf16 or FP8 storage) on one device; the graph does
+ * not own them and must be destroyed before they are.  Returns NULL on failure (dms_last_error()
  * gives the code; stream capture must not be active on the calling thread).
  *
  * dms_step_graph_launch enqueues one step on `stream`: the result equals

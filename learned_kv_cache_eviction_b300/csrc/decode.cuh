@@ -224,6 +224,21 @@ static __device__ __noinline__ void patch_new_row(const DecodeArgs& a, uint4* Kt
   __syncwarp();
 }
 
+// The same for FP8 storage: the new token's rows are quantized exactly as the
+// append stores them (quantize_kv_rows) into row j of the staged K tile (D
+// codes + the scale chunk) and V tile (D codes).  Called by the whole warp.
+template <int D>
+static __device__ __noinline__ void patch_new_row_fp8(const DecodeArgs& a, uint8_t* Kt, uint8_t* Vt, int i, int j,
+                                                      int lane) {
+  constexpr int CH = D / 8;
+  uint4 x = make_uint4(0u, 0u, 0u, 0u);
+  if (lane < CH) x = __ldg(a.k_new + static_cast<size_t>(i) * CH + lane);
+  else if (lane < 2 * CH) x = __ldg(a.v_new + static_cast<size_t>(i) * CH + lane - CH);
+  quantize_kv_rows<D>(x, Kt + j * (D + 16), Vt + j * D, lane);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+}
+
 // Fused step started early (DecodeArgs::early): head x's state as the step
 // sees it, derived without reading anything the previous step wrote.  From
 // the lengths after t - 1 appends and the ring entries of t - 1 - w and t - w:
@@ -472,7 +487,6 @@ __device__ __forceinline__ bool merge_partials(const DecodeArgs& a, size_t base,
 template <int D, int G, bool FUSED, int KVF = kKvBf16>
 __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_kernel(const DecodeArgs a) {
   using Sh = DecodeShape<D, G, KVF>;
-  static_assert(!(FUSED && Sh::FP8), "the fused step stores bf16 rows");
   constexpr int NW = Sh::NW, TK = Sh::TK, NST = Sh::NST, CH = Sh::CH, HCH = Sh::HCH, EL = Sh::EL;
   constexpr int ROWB_K = Sh::ROWB_K, ROWB_V = Sh::ROWB_V, TILEB_K = Sh::TILEB_K, TILEB_V = Sh::TILEB_V;
   constexpr int QHALF = Sh::QHALF, QROW = Sh::QROW, PROW = Sh::PROW;
@@ -570,9 +584,15 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
       else atomicOr(a.err, kErrBitCapacity);
     }
     if (s_new >= 0) {
-      const size_t row = (static_cast<size_t>(i) * a.cap + s_new) * CH;
-      if (lane < CH) a.K_w[row + (lane ^ (s_new & 7))] = rowc;
-      else if (lane < 2 * CH) a.V_w[row + lane - CH] = rowc;
+      if constexpr (Sh::FP8) {
+        const size_t slot = static_cast<size_t>(i) * a.cap + s_new;
+        quantize_kv_rows<D>(rowc, reinterpret_cast<uint8_t*>(a.K_w) + slot * (D + 16),
+                            reinterpret_cast<uint8_t*>(a.V_w) + slot * D, lane);
+      } else {
+        const size_t row = (static_cast<size_t>(i) * a.cap + s_new) * CH;
+        if (lane < CH) a.K_w[row + (lane ^ (s_new & 7))] = rowc;
+        else if (lane < 2 * CH) a.V_w[row + lane - CH] = rowc;
+      }
     }
   };
   auto load_new_row = [&](int i) {
@@ -827,9 +847,13 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
 
     if constexpr (FUSED) {
       const int sw = fx[Sh::FX_SEG];  // reloaded after the wait (the wait clobbers memory)
-      if (static_cast<unsigned>(sw - s0) < static_cast<unsigned>(cnt))
-        patch_new_row(a, reinterpret_cast<uint4*>(Ks + buf * TILEB_K), reinterpret_cast<uint4*>(Vs + buf * TILEB_V),
-                      real_head(seg_i), sw - s0, sw, CH, lane);
+      if (static_cast<unsigned>(sw - s0) < static_cast<unsigned>(cnt)) {
+        if constexpr (Sh::FP8)
+          patch_new_row_fp8<D>(a, Ks + buf * TILEB_K, Vs + buf * TILEB_V, real_head(seg_i), sw - s0, lane);
+        else
+          patch_new_row(a, reinterpret_cast<uint4*>(Ks + buf * TILEB_K), reinterpret_cast<uint4*>(Vs + buf * TILEB_V),
+                        real_head(seg_i), sw - s0, sw, CH, lane);
+      }
     }
 
     // ---- QK and online softmax (base 2) ----

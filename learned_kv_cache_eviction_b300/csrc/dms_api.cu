@@ -268,27 +268,31 @@ int launch_prefill_d(dms_cache* c, const dms::PrefillArgs& a, int G, cudaStream_
   }
 }
 
-// decode_attr for the cache's head dim and group size (fused kernel).
-template <int D>
-int fused_attr_d(const dms_cache* c, int G) {
+// decode_attr for the cache's head dim, group size and format (fused kernel).
+template <int D, int KVF>
+int fused_attr_k(const dms_cache* c, int G) {
   switch (G) {
-    case 1: return decode_attr<D, 1, true, dms::kKvBf16>(c);
-    case 2: return decode_attr<D, 2, true, dms::kKvBf16>(c);
-    case 3: return decode_attr<D, 3, true, dms::kKvBf16>(c);
-    case 4: return decode_attr<D, 4, true, dms::kKvBf16>(c);
-    case 5: return decode_attr<D, 5, true, dms::kKvBf16>(c);
-    case 6: return decode_attr<D, 3, true, dms::kKvBf16>(c);
-    case 7: return decode_attr<D, 7, true, dms::kKvBf16>(c);
-    case 8: return decode_attr<D, 4, true, dms::kKvBf16>(c);
+    case 1: return decode_attr<D, 1, true, KVF>(c);
+    case 2: return decode_attr<D, 2, true, KVF>(c);
+    case 3: return decode_attr<D, 3, true, KVF>(c);
+    case 4: return decode_attr<D, 4, true, KVF>(c);
+    case 5: return decode_attr<D, 5, true, KVF>(c);
+    case 6: return decode_attr<D, 3, true, KVF>(c);
+    case 7: return decode_attr<D, 7, true, KVF>(c);
+    case 8: return decode_attr<D, 4, true, KVF>(c);
     default: return DMS_ERR_INVALID_ARG;
   }
 }
+template <int D>
+int fused_attr_d(const dms_cache* c, int G) {
+  return c->kvf == DMS_KV_FP8_E4M3 ? fused_attr_k<D, dms::kKvFp8>(c, G) : fused_attr_k<D, dms::kKvBf16>(c, G);
+}
 
-// Decode launch for the cache's storage format.
+// Decode launch for the cache's storage format (plain, or fused with `in`).
 template <int D, bool FUSED>
 int launch_decode_f(dms_cache* c, const void* q, float* out, float scale, int G, cudaStream_t st,
                     const StepInput* in = nullptr) {
-  return c->kvf == DMS_KV_FP8_E4M3 ? launch_decode_d<D, false, dms::kKvFp8>(c, q, out, scale, G, st)
+  return c->kvf == DMS_KV_FP8_E4M3 ? launch_decode_d<D, FUSED, dms::kKvFp8>(c, q, out, scale, G, st, in)
                                    : launch_decode_d<D, FUSED, dms::kKvBf16>(c, q, out, scale, G, st, in);
 }
 
@@ -378,8 +382,8 @@ struct RoundLayout {
 };
 
 // FP8 caches: the chunked prefill as its definition states it, C rounds of
-// (append token c, decode token c's query), on the FP8 append and decode
-// kernels.  Token c's rows are gathered from the chunk layouts into the
+// (append token c, decode token c's query), each one launch of the fused FP8
+// step kernel.  Token c's rows are gathered from the chunk layouts into the
 // cache's round buffer with pitched copies, and its output row is scattered
 // back.  Exact by construction; one decode launch per token.
 int prefill_by_rounds(dms_cache* c, const void* q, const void* k, const void* v, const float* logits, int chunk,
@@ -403,13 +407,14 @@ int prefill_by_rounds(dms_cache* c, const void* q, const void* k, const void* v,
       cudaGetLastError();
       return DMS_ERR_CUDA;
     }
-    int rc = launch_append(c, rb + lay.k, rb + lay.v, reinterpret_cast<const float*>(rb + lay.logit), st);
+    // one fused step (append + decode) per token
+    float* o = reinterpret_cast<float*>(rb + lay.out);
+    const StepInput in{reinterpret_cast<const uint4*>(rb + lay.k), reinterpret_cast<const uint4*>(rb + lay.v),
+                       reinterpret_cast<const float*>(rb + lay.logit), nullptr, false};
+    const int rc = c->D == 128 ? launch_decode_f<128, true>(c, rb + lay.q, o, scale, G, st, &in)
+                               : launch_decode_f<64, true>(c, rb + lay.q, o, scale, G, st, &in);
     if (rc != DMS_OK) return rc;
     c->t += 1;
-    float* o = reinterpret_cast<float*>(rb + lay.out);
-    rc = c->D == 128 ? launch_decode_f<128, false>(c, rb + lay.q, o, scale, G, st)
-                     : launch_decode_f<64, false>(c, rb + lay.q, o, scale, G, st);
-    if (rc != DMS_OK) return rc;
     if (cudaMemcpy2DAsync(out + t * D, C * D * 4, o, D * 4, D * 4, rows_q, cudaMemcpyDeviceToDevice, st) !=
         cudaSuccess) {
       cudaGetLastError();
@@ -652,20 +657,10 @@ int dms_step(dms_cache_t* c, const void* k, const void* v, const float* evict_lo
     return DMS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int G = q_heads / c->H;
-  if (c->kvf == DMS_KV_FP8_E4M3) {
-    // fp8 caches: the append kernel, then the decode kernel
-    int rc = launch_append(c, k, v, evict_logit, st);
-    if (rc != DMS_OK) return rc;
-    c->t += 1;
-    c->single_prev = true;
-    c->t_dev_synced = false;
-    return c->D == 128 ? launch_decode_f<128, false>(c, q, out, scale, G, st)
-                       : launch_decode_f<64, false>(c, q, out, scale, G, st);
-  }
-  // bf16: one launch.  The decode kernel appends the token (into generations of
-  // the state that the step does not read) and attends over the cache after
-  // the append; after a one-token advance it starts before the previous launch
-  // has finished.
+  // One launch (bf16 or FP8 storage).  The decode kernel appends the token
+  // (into generations of the state that the step does not read; FP8 caches
+  // quantize it) and attends over the cache after the append; after a
+  // one-token advance it starts before the previous launch has finished.
   const StepInput in{static_cast<const uint4*>(k), static_cast<const uint4*>(v), evict_logit, nullptr,
                      step_can_start_early(c)};
   const int rc = c->D == 128 ? launch_decode_f<128, true>(c, q, out, scale, G, st, &in)
@@ -767,7 +762,7 @@ dms_step_graph_t* dms_step_graph_create(dms_cache_t* const* caches, int n, const
       g_last_error = DMS_ERR_BAD_HANDLE;
       return nullptr;
     }
-    if (!seen.insert(c).second || c->kvf != DMS_KV_BF16 || c->device != caches[0]->device ||
+    if (!seen.insert(c).second || c->device != caches[0]->device ||
         q_heads % c->H != 0 || q_heads / c->H > DMS_MAX_GROUP || !k[i] || !v[i] || !evict_logit[i] || !q[i] ||
         !out[i] || !aligned16(k[i]) || !aligned16(v[i]) || !aligned16(evict_logit[i]) || !aligned16(q[i]) ||
         !aligned16(out[i]))
@@ -810,8 +805,8 @@ dms_step_graph_t* dms_step_graph_create(dms_cache_t* const* caches, int n, const
       const StepInput in{static_cast<const uint4*>(k[i]), static_cast<const uint4*>(v[i]), evict_logit[i], c->t_dev,
                          i > 0 && c->w >= 2};
       const int G = q_heads / c->H;
-      rc = c->D == 128 ? launch_decode_d<128, true, dms::kKvBf16>(c, q[i], out[i], scale, G, st, &in)
-                       : launch_decode_d<64, true, dms::kKvBf16>(c, q[i], out[i], scale, G, st, &in);
+      rc = c->D == 128 ? launch_decode_f<128, true>(c, q[i], out[i], scale, G, st, &in)
+                       : launch_decode_f<64, true>(c, q[i], out[i], scale, G, st, &in);
     }
     if (rc == DMS_OK) rc = launch_pdl(dms::advance_positions_kernel, dim3(1), dim3(32), 0, st, sg->pos, n);
     cudaGraph_t graph = nullptr;
@@ -863,10 +858,8 @@ int dms_step_graph_launch(dms_step_graph_t* sg, void* stream) {
       const StepInput in{static_cast<const uint4*>(sg->k[i]), static_cast<const uint4*>(sg->v[i]), sg->logit[i],
                          nullptr, false};
       const int G = sg->q_heads / c->H;
-      const int rc = c->D == 128 ? launch_decode_d<128, true, dms::kKvBf16>(c, sg->q[i], sg->out[i], sg->scale, G,
-                                                                           st, &in)
-                                 : launch_decode_d<64, true, dms::kKvBf16>(c, sg->q[i], sg->out[i], sg->scale, G,
-                                                                          st, &in);
+      const int rc = c->D == 128 ? launch_decode_f<128, true>(c, sg->q[i], sg->out[i], sg->scale, G, st, &in)
+                                 : launch_decode_f<64, true>(c, sg->q[i], sg->out[i], sg->scale, G, st, &in);
       if (rc != DMS_OK) return rc;
       c->t += 1;
       c->single_prev = true;

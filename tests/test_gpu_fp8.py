@@ -159,6 +159,63 @@ def test_fp8_step_equals_append_then_decode():
     assert a.status() == b.status() == dms.DMS_OK
 
 
+def test_fp8_back_to_back_steps_and_graph():
+    """FP8 storage through the one-launch step: dms_step calls with no host
+    synchronisation between them (each started early under the previous one),
+    and a 2-layer step graph replayed per token, give outputs, codes and scales
+    equal, bit for bit, to dms_append + dms_decode_attention per token."""
+    wl = _wl(2, 16, 2, 128, 16, 400, ("normal", 0.8, 1.0), seed=29)
+    T0, T = 40, 240
+    L = 2
+    data = [tuple(x.cuda() for x in W.kv_range(wl, layer, 0, T)) + (W.q_range(wl, layer, 0, T).cuda(),)
+            for layer in range(L)]
+    ref = [dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w, kv_format="fp8") for _ in range(L)]
+    got = [dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w, kv_format="fp8") for _ in range(L)]
+    for layer in range(L):
+        k, v, lg, _ = data[layer]
+        for c in (ref[layer], got[layer]):
+            c.append_chunk(k[:, :, :T0].contiguous(), v[:, :, :T0].contiguous(), lg[:, :, :T0].contiguous())
+    kb = [torch.empty((wl.B, wl.Hkv, wl.D), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    vb = [torch.empty_like(x) for x in kb]
+    lb = [torch.empty((wl.B, wl.Hkv), dtype=torch.float32, device="cuda") for _ in range(L)]
+    qb = [torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    ob = [torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda") for _ in range(L)]
+    graph = dms.DmsStepGraph(got, kb, vb, lb, qb, ob, wl.scale)
+    hist_got = torch.zeros((T, L, wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    hist_ref = torch.zeros_like(hist_got)
+    for t in range(T0, T):
+        if t < (T0 + T) // 2:  # first half: dms_step per layer, back to back
+            for layer in range(L):
+                k, v, lg, q = data[layer]
+                got[layer].step(k[:, :, t].contiguous(), v[:, :, t].contiguous(), lg[:, :, t].contiguous(),
+                                q[:, :, t].contiguous(), hist_got[t, layer], scale=wl.scale)
+        else:  # second half: the graph
+            for layer in range(L):
+                k, v, lg, q = data[layer]
+                kb[layer].copy_(k[:, :, t])
+                vb[layer].copy_(v[:, :, t])
+                lb[layer].copy_(lg[:, :, t])
+                qb[layer].copy_(q[:, :, t])
+            graph.launch()
+            for layer in range(L):
+                hist_got[t, layer].copy_(ob[layer])
+        for layer in range(L):
+            k, v, lg, q = data[layer]
+            ref[layer].append(k[:, :, t].contiguous(), v[:, :, t].contiguous(), lg[:, :, t].contiguous())
+            ref[layer].decode_attention(q[:, :, t].contiguous(), out=hist_ref[t, layer], scale=wl.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(hist_got, hist_ref)
+    for layer in range(L):
+        for x, y in zip(ref[layer].export_kv() + ref[layer].export_scales(),
+                        got[layer].export_kv() + got[layer].export_scales()):
+            assert torch.equal(x, y)
+        assert torch.equal(ref[layer].lengths(), got[layer].lengths())
+        assert ref[layer].status() == got[layer].status() == dms.DMS_OK
+    graph.close()
+    for c in ref + got:
+        c.close()
+
+
 def test_fp8_capacity_overflow_is_reported():
     wl = _wl(1, 4, 2, 64, 4, 10, ("const", -10.0))
     run = Fp8Run(wl, 14)

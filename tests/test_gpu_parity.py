@@ -630,13 +630,10 @@ def test_step_graph_equals_dms_step_per_layer(shape):
         assert torch.equal(ka, kr) and torch.equal(va, vr)
         assert got[layer].status() == dms.DMS_OK
     graph.close()
-    # refused: an fp8 cache, a cache listed twice
-    f = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w, kv_format="fp8")
-    with pytest.raises(dms.DmsError):
-        dms.DmsStepGraph([f], kb[:1], vb[:1], lb[:1], qb[:1], ob[:1], wl.scale)
+    # refused: a cache listed twice
     with pytest.raises(dms.DmsError):
         dms.DmsStepGraph([got[0], got[0]], kb[:2], vb[:2], lb[:2], qb[:2], ob[:2], wl.scale)
-    for c in ref + got + [f]:
+    for c in ref + got:
         c.close()
 
 
