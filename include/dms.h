@@ -197,6 +197,39 @@ int dms_decode_attention(dms_cache_t* cache, const void* q, float* out, float sc
 int dms_step(dms_cache_t* cache, const void* k, const void* v, const float* evict_logit, const void* q, float* out,
              float scale, int q_heads, void* stream);
 
+/*
+ * dms_step with its inputs read from, and its output written to, HOST memory:
+ * the call a serving loop makes when the token's rows arrive from, and the
+ * attention output goes back to, the host.  Same result as dms_step on the
+ * same rows, bit for bit (the same kernel runs on device copies of them).
+ *   k, v         bf16 [batch][kv_heads][head_dim]   host memory
+ *   evict_logit  fp32 [batch][kv_heads]             host memory
+ *   q            bf16 [batch][q_heads][head_dim]    host memory
+ *   out          fp32 [batch][q_heads][head_dim]    host memory, written
+ * The cache keeps two sets of device rows and two copy streams of its own,
+ * made (with cudaMalloc) on the first call.  Call i uses set i % 2: its
+ * host->device copies wait only for the step of call i - 2, so they overlap
+ * the step of call i - 1, and its device->host copy overlaps the step of
+ * call i + 1.  The step itself runs on `stream`, after its own copies in.
+ * Everything is asynchronous:
+ *  - the host input buffers must stay unchanged, and `out` unread, until the
+ *    call's copies are done: dms_step_host_join(cache, s) makes stream s wait
+ *    for every copy out enqueued so far, after which a synchronize of s (or
+ *    an event recorded on it) says that all outputs are in host memory;
+ *  - pinned (page-locked) host memory lets the copies overlap the steps;
+ *    with pageable memory the copies are correct but serialize with the host.
+ * Not allowed while `stream` is being captured into a CUDA graph
+ * (DMS_ERR_INVALID_ARG).  Device pointers are refused (DMS_ERR_INVALID_ARG):
+ * use dms_step for rows already on the device.
+ */
+int dms_step_host(dms_cache_t* cache, const void* k, const void* v, const float* evict_logit, const void* q,
+                  float* out, float scale, int q_heads, void* stream);
+
+/* Make `stream` wait for every device->host copy that dms_step_host has
+ * enqueued on this cache so far.  Enqueues only waits; DMS_OK if no host step
+ * was made. */
+int dms_step_host_join(dms_cache_t* cache, void* stream);
+
 /* Copy the retained length of every (sequence, KV head) into out_dev
  * (int32 [batch][kv_heads], device memory), stream-ordered. */
 int dms_cache_lengths(dms_cache_t* cache, int32_t* out_dev, void* stream);

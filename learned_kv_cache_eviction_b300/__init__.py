@@ -22,5 +22,7 @@ from .dms import (  # noqa: F401
     dms_step_graph_create,
     dms_step_graph_destroy,
     dms_step_graph_launch,
+    dms_step_host,
+    dms_step_host_join,
     load_library,
 )

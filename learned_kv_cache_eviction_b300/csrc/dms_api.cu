@@ -42,6 +42,23 @@ struct dms_cache {
   // FP8 caches: one token's rows for the prefill's rounds of append + decode
   // (q bf16 [B][8 H][D] | out fp32 [B][8 H][D] | k, v bf16 [NH][D] | logit fp32 [NH]).
   uint8_t* round_buf;
+  // Steps from host buffers (dms_step_host), made on first use.
+  struct dms_host_pipe* host_pipe;
+};
+
+// Two sets of device rows for steps whose inputs and output live in host
+// memory, with a copy-in and a copy-out stream.  Call i uses set i % 2: its
+// host->device copies wait only for the kernel of call i - 2 (which read that
+// set), so they run under the kernel of call i - 1; its device->host copy runs
+// under the kernel of call i + 1.  in_done, kern_done and out_done are the
+// events that order the three streams; used[s] says whether set s has been
+// through a call (so that its events have been recorded).
+struct dms_host_pipe {
+  cudaStream_t in_st = nullptr, out_st = nullptr;
+  cudaEvent_t in_done[2] = {}, kern_done[2] = {}, out_done[2] = {};
+  bool used[2] = {false, false};
+  uint8_t* buf[2] = {nullptr, nullptr};  // each laid out as RoundLayout
+  int next = 0;
 };
 
 namespace {
@@ -353,7 +370,22 @@ struct dms_step_graph {
 
 namespace {
 
+void free_host_pipe(dms_host_pipe* p) {
+  if (p == nullptr) return;
+  for (int s = 0; s < 2; ++s) {
+    if (p->in_done[s]) cudaEventDestroy(p->in_done[s]);
+    if (p->kern_done[s]) cudaEventDestroy(p->kern_done[s]);
+    if (p->out_done[s]) cudaEventDestroy(p->out_done[s]);
+    cudaFree(p->buf[s]);
+  }
+  if (p->in_st) cudaStreamDestroy(p->in_st);
+  if (p->out_st) cudaStreamDestroy(p->out_st);
+  delete p;
+}
+
 void free_cache_memory(dms_cache* c) {
+  free_host_pipe(c->host_pipe);
+  c->host_pipe = nullptr;
   cudaFree(c->view.K);
   cudaFree(c->view.V);
   cudaFree(c->view.slot_pos);
@@ -422,6 +454,57 @@ int prefill_by_rounds(dms_cache* c, const void* q, const void* k, const void* v,
     }
   }
   return DMS_OK;
+}
+
+// The fused step (append token t, decode its query) on device rows whose
+// pointers the caller has checked; advances the host position.
+int step_launch(dms_cache* c, const void* k, const void* v, const float* evict_logit, const void* q, float* out,
+                float scale, int G, cudaStream_t st) {
+  // One launch (bf16 or FP8 storage).  The decode kernel appends the token
+  // (into generations of the state that the step does not read; FP8 caches
+  // quantize it) and attends over the cache after the append; after a
+  // one-token advance it starts before the previous launch has finished.
+  const StepInput in{static_cast<const uint4*>(k), static_cast<const uint4*>(v), evict_logit, nullptr,
+                     step_can_start_early(c)};
+  const int rc = c->D == 128 ? launch_decode_f<128, true>(c, q, out, scale, G, st, &in)
+                             : launch_decode_f<64, true>(c, q, out, scale, G, st, &in);
+  if (rc != DMS_OK) return rc;
+  c->t += 1;
+  c->single_prev = true;
+  c->t_dev_synced = false;
+  return DMS_OK;
+}
+
+// The host-buffer pipeline of a cache, made on its first use.
+dms_host_pipe* host_pipe(dms_cache* c) {
+  if (c->host_pipe != nullptr) return c->host_pipe;
+  dms_host_pipe* p = new (std::nothrow) dms_host_pipe();
+  if (p == nullptr) return nullptr;
+  const size_t bytes = RoundLayout(c).total;
+  bool ok = cudaStreamCreateWithFlags(&p->in_st, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p->out_st, cudaStreamNonBlocking) == cudaSuccess;
+  for (int s = 0; s < 2 && ok; ++s)
+    ok = cudaEventCreateWithFlags(&p->in_done[s], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p->kern_done[s], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p->out_done[s], cudaEventDisableTiming) == cudaSuccess &&
+         cudaMalloc(&p->buf[s], bytes) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    free_host_pipe(p);
+    return nullptr;
+  }
+  c->host_pipe = p;
+  return p;
+}
+
+// Host memory that a copy may read or write (pinned, or plain pageable memory).
+bool host_pointer_ok(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return true;  // unknown to CUDA: pageable host memory
+  }
+  return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
 }
 
 }  // namespace
@@ -655,20 +738,79 @@ int dms_step(dms_cache_t* c, const void* k, const void* v, const float* evict_lo
       !device_pointer_ok(evict_logit, c->device) || !device_pointer_ok(q, c->device) ||
       !device_pointer_ok(out, c->device))
     return DMS_ERR_INVALID_ARG;
+  return step_launch(c, k, v, evict_logit, q, out, scale, q_heads / c->H, static_cast<cudaStream_t>(stream));
+}
+
+int dms_step_host(dms_cache_t* c, const void* k, const void* v, const float* evict_logit, const void* q, float* out,
+                  float scale, int q_heads, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  if (!k || !v || !evict_logit || !q || !out || q_heads < 1 || q_heads % c->H != 0 ||
+      q_heads / c->H > DMS_MAX_GROUP || !std::isfinite(scale))
+    return DMS_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return DMS_ERR_CUDA;
+  if (!host_pointer_ok(k) || !host_pointer_ok(v) || !host_pointer_ok(evict_logit) || !host_pointer_ok(q) ||
+      !host_pointer_ok(out))
+    return DMS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int G = q_heads / c->H;
-  // One launch (bf16 or FP8 storage).  The decode kernel appends the token
-  // (into generations of the state that the step does not read; FP8 caches
-  // quantize it) and attends over the cache after the append; after a
-  // one-token advance it starts before the previous launch has finished.
-  const StepInput in{static_cast<const uint4*>(k), static_cast<const uint4*>(v), evict_logit, nullptr,
-                     step_can_start_early(c)};
-  const int rc = c->D == 128 ? launch_decode_f<128, true>(c, q, out, scale, G, st, &in)
-                             : launch_decode_f<64, true>(c, q, out, scale, G, st, &in);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return DMS_ERR_INVALID_ARG;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return DMS_ERR_INVALID_ARG;
+  dms_host_pipe* p = host_pipe(c);
+  if (p == nullptr) return DMS_ERR_CUDA;
+  const RoundLayout lay(c);
+  const int s = p->next;
+  uint8_t* b = p->buf[s];
+  const size_t D = static_cast<size_t>(c->D), NH = static_cast<size_t>(c->NH);
+  const size_t q_bytes = static_cast<size_t>(c->B) * q_heads * D * 2;
+  // copy in, after the kernel that last read this set
+  bool ok = !p->used[s] || cudaStreamWaitEvent(p->in_st, p->kern_done[s], 0) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(b + lay.k, k, NH * D * 2, cudaMemcpyHostToDevice, p->in_st) == cudaSuccess &&
+       cudaMemcpyAsync(b + lay.v, v, NH * D * 2, cudaMemcpyHostToDevice, p->in_st) == cudaSuccess &&
+       cudaMemcpyAsync(b + lay.logit, evict_logit, NH * 4, cudaMemcpyHostToDevice, p->in_st) == cudaSuccess &&
+       cudaMemcpyAsync(b + lay.q, q, q_bytes, cudaMemcpyHostToDevice, p->in_st) == cudaSuccess &&
+       cudaEventRecord(p->in_done[s], p->in_st) == cudaSuccess;
+  // the step, after its inputs have landed and the copy-out that last read this set's output
+  ok = ok && cudaStreamWaitEvent(st, p->in_done[s], 0) == cudaSuccess &&
+       (!p->used[s] || cudaStreamWaitEvent(st, p->out_done[s], 0) == cudaSuccess);
+  if (!ok) {
+    cudaGetLastError();
+    return DMS_ERR_CUDA;
+  }
+  float* o = reinterpret_cast<float*>(b + lay.out);
+  const int rc = step_launch(c, b + lay.k, b + lay.v, reinterpret_cast<const float*>(b + lay.logit), b + lay.q, o,
+                             scale, q_heads / c->H, st);
   if (rc != DMS_OK) return rc;
-  c->t += 1;
-  c->single_prev = true;
-  c->t_dev_synced = false;
+  // copy out, after the step
+  ok = cudaEventRecord(p->kern_done[s], st) == cudaSuccess &&
+       cudaStreamWaitEvent(p->out_st, p->kern_done[s], 0) == cudaSuccess &&
+       cudaMemcpyAsync(out, o, static_cast<size_t>(c->B) * q_heads * D * 4, cudaMemcpyDeviceToHost, p->out_st) ==
+           cudaSuccess &&
+       cudaEventRecord(p->out_done[s], p->out_st) == cudaSuccess;
+  p->used[s] = true;
+  p->next = s ^ 1;
+  if (!ok) {
+    cudaGetLastError();
+    return DMS_ERR_CUDA;
+  }
+  return DMS_OK;
+}
+
+int dms_step_host_join(dms_cache_t* c, void* stream) {
+  if (!is_live(c)) return DMS_ERR_BAD_HANDLE;
+  dms_host_pipe* p = c->host_pipe;
+  if (p == nullptr) return DMS_OK;
+  DeviceGuard g(c->device);
+  if (!g.ok) return DMS_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int s = 0; s < 2; ++s)
+    if (p->used[s] && cudaStreamWaitEvent(st, p->out_done[s], 0) != cudaSuccess) {
+      cudaGetLastError();
+      return DMS_ERR_CUDA;
+    }
   return DMS_OK;
 }
 

@@ -46,6 +46,8 @@ SIGNATURES = {
     "dms_decode_attention": (_I, [_P, _P, _P, ctypes.c_float, _I, _P]),
     "dms_prefill": (_I, [_P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _P]),
     "dms_step": (_I, [_P, _P, _P, _P, _P, _P, ctypes.c_float, _I, _P]),
+    "dms_step_host": (_I, [_P, _P, _P, _P, _P, _P, ctypes.c_float, _I, _P]),
+    "dms_step_host_join": (_I, [_P, _P]),
     "dms_cache_lengths": (_I, [_P, _P, _P]),
     "dms_cache_slot_positions": (_I, [_P, _P, _P]),
     "dms_cache_export_kv": (_I, [_P, _P, _P, _P]),
@@ -208,6 +210,31 @@ class DmsCache:
                                   out.data_ptr(), scale, Hq, _stream_handle(stream)), "dms_step")
         return out
 
+    def step_host(self, k: torch.Tensor, v: torch.Tensor, evict_logit: torch.Tensor, q: torch.Tensor,
+                  out: torch.Tensor, scale: float | None = None, stream=None) -> torch.Tensor:
+        """dms_step with host tensors (dms_step_host): k, v [B][Hkv][D] bf16,
+        evict_logit [B][Hkv] fp32, q [B][Hq][D] bf16 and out [B][Hq][D] fp32,
+        all on the CPU (pinned memory lets the copies overlap the steps).
+        Asynchronous: `out` holds the result once host_join(stream) has been
+        called and the stream synchronized."""
+        B, H, D = self.batch, self.kv_heads, self.head_dim
+        Hq = q.shape[1] if q.dim() == 3 else -1
+        cpu = torch.device("cpu")
+        _need(k, "k", torch.bfloat16, (B, H, D), cpu)
+        _need(v, "v", torch.bfloat16, (B, H, D), cpu)
+        _need(evict_logit, "evict_logit", torch.float32, (B, H), cpu)
+        _need(q, "q", torch.bfloat16, (B, Hq, D), cpu)
+        _need(out, "out", torch.float32, (B, Hq, D), cpu)
+        scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+        _check(self._lib.dms_step_host(self.handle, k.data_ptr(), v.data_ptr(), evict_logit.data_ptr(),
+                                       q.data_ptr(), out.data_ptr(), scale, Hq, _stream_handle(stream)),
+               "dms_step_host")
+        return out
+
+    def host_join(self, stream=None) -> None:
+        """Make `stream` wait for every output copy of step_host so far."""
+        _check(self._lib.dms_step_host_join(self.handle, _stream_handle(stream)), "dms_step_host_join")
+
     def decode_attention(self, q: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,
                          stream=None) -> torch.Tensor:
         B, D = self.batch, self.head_dim
@@ -333,6 +360,14 @@ def dms_decode_attention(cache: DmsCache, q, out=None, scale=None, stream=None):
 
 def dms_step(cache: DmsCache, k, v, evict_logit, q, out, scale=None, stream=None):
     return cache.step(k, v, evict_logit, q, out, scale, stream)
+
+
+def dms_step_host(cache: DmsCache, k, v, evict_logit, q, out, scale=None, stream=None):
+    return cache.step_host(k, v, evict_logit, q, out, scale, stream)
+
+
+def dms_step_host_join(cache: DmsCache, stream=None) -> None:
+    cache.host_join(stream)
 
 
 def dms_step_graph_create(caches, k, v, evict_logit, q, out, scale) -> DmsStepGraph:

@@ -53,6 +53,8 @@ def test_null_handle_rejected_without_device(lib):
     assert lib.dms_cache_export_scales(None, None, None, None) == dms.DMS_ERR_BAD_HANDLE
     assert lib.dms_cache_kv_format(None) == dms.DMS_ERR_BAD_HANDLE
     assert lib.dms_step(None, None, None, None, None, None, 1.0, 4, None) == dms.DMS_ERR_BAD_HANDLE
+    assert lib.dms_step_host(None, None, None, None, None, None, 1.0, 4, None) == dms.DMS_ERR_BAD_HANDLE
+    assert lib.dms_step_host_join(None, None) == dms.DMS_ERR_BAD_HANDLE
     assert lib.dms_step_graph_launch(None, None) == dms.DMS_ERR_BAD_HANDLE
     assert lib.dms_step_graph_create(None, 0, None, None, None, None, None, 1.0, 4) is None
     assert lib.dms_last_error() == dms.DMS_ERR_INVALID_ARG
