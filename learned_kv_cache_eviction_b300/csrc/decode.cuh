@@ -177,7 +177,37 @@ struct DecodeArgs {
   // each length is clamped to [0, cap] before use, and a clamped value latches
   // kErrBitLength, so that a bad length can never send a copy past a head's pool.
   int clamp_len;
+  // Fused step from host rows (dms_step_host): the step's k, v, logit and q
+  // rows are copied in, and its output copied out, on copy streams of their
+  // own, which write sequence numbers into host_flag[0] (rows landed) and
+  // host_flag[1] (the output rows read back) when they finish.  Before it
+  // reads an input or writes an output, every warp waits (bounded) until
+  // host_flag[0] >= in_need and host_flag[1] >= out_need (wrap-safe), so the
+  // launch needs no cross-stream dependency and keeps its early start.  Null
+  // for every other call.
+  const unsigned* host_flag;
+  unsigned in_need, out_need;
 };
+
+// Steps from host rows: wait until the copy streams have landed this step's
+// rows and read back the output rows this step will overwrite (DecodeArgs::
+// host_flag).  On the time limit it latches kErrBitTimeout and returns; the
+// step then reads stale rows but stays within its buffers.
+__device__ __forceinline__ void wait_host_rows(const DecodeArgs& a) {
+  if (a.host_flag == nullptr) return;
+  uint64_t t0 = 0;
+  while (true) {
+    const unsigned fi = ld_acquire_u32(a.host_flag), fo = ld_acquire_u32(a.host_flag + 1);
+    if (static_cast<int>(fi - a.in_need) >= 0 && static_cast<int>(fo - a.out_need) >= 0) return;
+    const uint64_t now = global_timer_ns();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > kWaitLimitNs) {
+      atomicOr(a.err, kErrBitTimeout);
+      return;
+    }
+  }
+}
 
 // Length of head x in a plain decode, clamped when the lengths come from the caller.
 __device__ __forceinline__ int plain_len(const DecodeArgs& a, int x) {
@@ -216,9 +246,9 @@ static __device__ __noinline__ int fused_new_slot_far(const DecodeArgs& a, int64
 static __device__ __noinline__ void patch_new_row(const DecodeArgs& a, uint4* Kt, uint4* Vt, int i, int j, int s_new,
                                                   int CH, int lane) {
   if (lane < CH) {
-    Kt[j * CH + (lane ^ (s_new & 7))] = __ldg(a.k_new + static_cast<size_t>(i) * CH + lane);
+    Kt[j * CH + (lane ^ (s_new & 7))] = __ldcg(a.k_new + static_cast<size_t>(i) * CH + lane);
   } else if (lane < 2 * CH) {
-    Vt[j * CH + lane - CH] = __ldg(a.v_new + static_cast<size_t>(i) * CH + lane - CH);
+    Vt[j * CH + lane - CH] = __ldcg(a.v_new + static_cast<size_t>(i) * CH + lane - CH);
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncwarp();
@@ -232,8 +262,8 @@ static __device__ __noinline__ void patch_new_row_fp8(const DecodeArgs& a, uint8
                                                       int lane) {
   constexpr int CH = D / 8;
   uint4 x = make_uint4(0u, 0u, 0u, 0u);
-  if (lane < CH) x = __ldg(a.k_new + static_cast<size_t>(i) * CH + lane);
-  else if (lane < 2 * CH) x = __ldg(a.v_new + static_cast<size_t>(i) * CH + lane - CH);
+  if (lane < CH) x = __ldcg(a.k_new + static_cast<size_t>(i) * CH + lane);
+  else if (lane < 2 * CH) x = __ldcg(a.v_new + static_cast<size_t>(i) * CH + lane - CH);
   quantize_kv_rows<D>(x, Kt + j * (D + 16), Vt + j * D, lane);
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncwarp();
@@ -501,6 +531,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   if (!early) {
     griddep_wait();
     griddep_launch_dependents();
+    if constexpr (FUSED) wait_host_rows(a);
   }
 
   // ---- prologue: prefix sums of the retained lengths, warp ranges ----
@@ -530,8 +561,8 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   if constexpr (FUSED) {
     if (!early && wg < a.NH) {
       if (lane < 2 * CH)
-        own_row = __ldg((lane < CH ? a.k_new : a.v_new) + static_cast<size_t>(wg) * CH + (lane % CH));
-      own_logit = __ldg(a.logit_new + wg);
+        own_row = __ldcg((lane < CH ? a.k_new : a.v_new) + static_cast<size_t>(wg) * CH + (lane % CH));
+      own_logit = __ldcg(a.logit_new + wg);
     }
   }
   // The scan reads each head's length (and, fused, the ring entry of t - w) once
@@ -597,7 +628,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   };
   auto load_new_row = [&](int i) {
     uint4 rowc = make_uint4(0u, 0u, 0u, 0u);
-    if (lane < 2 * CH) rowc = __ldg((lane < CH ? a.k_new : a.v_new) + static_cast<size_t>(i) * CH + (lane % CH));
+    if (lane < 2 * CH) rowc = __ldcg((lane < CH ? a.k_new : a.v_new) + static_cast<size_t>(i) * CH + (lane % CH));
     return rowc;
   };
   if constexpr (FUSED) {
@@ -606,7 +637,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
         const int i = static_cast<int>(x);
         const bool own = x == wg;
         append_head(i, sn[i], ln[i], own ? own_row : load_new_row(i),
-                    own ? own_logit : __ldg(a.logit_new + i));
+                    own ? own_logit : __ldcg(a.logit_new + i));
       }
     }
   }
@@ -717,7 +748,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
 #pragma unroll
     for (int u = 0; u < QV; ++u) {
       const int y = lane + 32 * u;
-      if (y < G * D / 8) qpre[u] = __ldg(qsrc + y);
+      if (y < G * D / 8) qpre[u] = __ldcg(qsrc + y);
     }
     ++nq_issued;
   };
@@ -751,13 +782,14 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
       }
       griddep_wait();
       griddep_launch_dependents();
+      wait_host_rows(a);
       for (int64_t x = wg; x < a.NH; x += nwarps) {
         const int i = static_cast<int>(x);
         if (x == wg) {
-          append_head(i, own_sn, own_L, load_new_row(i), __ldg(a.logit_new + i));
+          append_head(i, own_sn, own_L, load_new_row(i), __ldcg(a.logit_new + i));
         } else {
           const EarlyHead eh = early_head(a, t_step, i);
-          append_head(i, eh.s_new, eh.L, load_new_row(i), __ldg(a.logit_new + i));
+          append_head(i, eh.s_new, eh.L, load_new_row(i), __ldcg(a.logit_new + i));
         }
       }
       if (!active) return;

@@ -2,6 +2,7 @@
 // lifetime, argument checks, kernel dispatch.  All compute runs in the
 // kernels of append.cuh and decode.cuh; this file only validates, allocates
 // at creation time and launches.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -50,14 +51,20 @@ struct dms_cache {
 // memory, with a copy-in and a copy-out stream.  Call i uses set i % 2: its
 // host->device copies wait only for the kernel of call i - 2 (which read that
 // set), so they run under the kernel of call i - 1; its device->host copy runs
-// under the kernel of call i + 1.  in_done, kern_done and out_done are the
-// events that order the three streams; used[s] says whether set s has been
-// through a call (so that its events have been recorded).
+// under the kernel of call i + 1.  The copy streams wait for kernels through
+// the kern_done events; the kernels wait for the copy streams through sequence
+// numbers that the copy streams write into flags (stream memory writes) and
+// the kernel polls (DecodeArgs::host_flag), so that the compute stream holds
+// nothing but the step kernels and each keeps its early start.
+typedef CUresult (*StreamWriteValue32Fn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
 struct dms_host_pipe {
   cudaStream_t in_st = nullptr, out_st = nullptr;
-  cudaEvent_t in_done[2] = {}, kern_done[2] = {}, out_done[2] = {};
+  cudaEvent_t kern_done[2] = {}, out_done[2] = {};
   bool used[2] = {false, false};
   uint8_t* buf[2] = {nullptr, nullptr};  // each laid out as RoundLayout
+  unsigned* flags = nullptr;             // [2 sets][rows landed, output read back]
+  unsigned seq[2] = {0, 0};              // calls made on each set
+  StreamWriteValue32Fn write_value = nullptr;
   int next = 0;
 };
 
@@ -139,6 +146,9 @@ struct StepInput {
   const float* logit;
   const int64_t* t_dev;
   bool early;
+  // steps from host rows: the set's sequence flags and the values to wait for
+  const unsigned* host_flag = nullptr;
+  unsigned in_need = 0, out_need = 0;
 };
 
 // May the fused step of cache c at its current position start early?  Needs
@@ -225,6 +235,9 @@ int launch_decode_t(dms_cache* c, const void* q, float* out, float scale, cudaSt
     a.len_w = c->view.len;
     a.t_dev = in->t_dev;
     a.early = in->early ? 1 : 0;
+    a.host_flag = in->host_flag;
+    a.in_need = in->in_need;
+    a.out_need = in->out_need;
   }
   return launch_pdl(dms::decode_kernel<D, G, FUSED, KVF>, dim3(grid), dim3(Sh::NW * 32), Sh::SMEM, st, a);
 }
@@ -373,11 +386,11 @@ namespace {
 void free_host_pipe(dms_host_pipe* p) {
   if (p == nullptr) return;
   for (int s = 0; s < 2; ++s) {
-    if (p->in_done[s]) cudaEventDestroy(p->in_done[s]);
     if (p->kern_done[s]) cudaEventDestroy(p->kern_done[s]);
     if (p->out_done[s]) cudaEventDestroy(p->out_done[s]);
     cudaFree(p->buf[s]);
   }
+  cudaFree(p->flags);
   if (p->in_st) cudaStreamDestroy(p->in_st);
   if (p->out_st) cudaStreamDestroy(p->out_st);
   delete p;
@@ -459,13 +472,17 @@ int prefill_by_rounds(dms_cache* c, const void* q, const void* k, const void* v,
 // The fused step (append token t, decode its query) on device rows whose
 // pointers the caller has checked; advances the host position.
 int step_launch(dms_cache* c, const void* k, const void* v, const float* evict_logit, const void* q, float* out,
-                float scale, int G, cudaStream_t st) {
+                float scale, int G, cudaStream_t st, const unsigned* host_flag = nullptr, unsigned in_need = 0,
+                unsigned out_need = 0) {
   // One launch (bf16 or FP8 storage).  The decode kernel appends the token
   // (into generations of the state that the step does not read; FP8 caches
   // quantize it) and attends over the cache after the append; after a
   // one-token advance it starts before the previous launch has finished.
-  const StepInput in{static_cast<const uint4*>(k), static_cast<const uint4*>(v), evict_logit, nullptr,
-                     step_can_start_early(c)};
+  StepInput in{static_cast<const uint4*>(k), static_cast<const uint4*>(v), evict_logit, nullptr,
+               step_can_start_early(c)};
+  in.host_flag = host_flag;
+  in.in_need = in_need;
+  in.out_need = out_need;
   const int rc = c->D == 128 ? launch_decode_f<128, true>(c, q, out, scale, G, st, &in)
                              : launch_decode_f<64, true>(c, q, out, scale, G, st, &in);
   if (rc != DMS_OK) return rc;
@@ -481,11 +498,18 @@ dms_host_pipe* host_pipe(dms_cache* c) {
   dms_host_pipe* p = new (std::nothrow) dms_host_pipe();
   if (p == nullptr) return nullptr;
   const size_t bytes = RoundLayout(c).total;
-  bool ok = cudaStreamCreateWithFlags(&p->in_st, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaStreamCreateWithFlags(&p->out_st, cudaStreamNonBlocking) == cudaSuccess;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult qr = cudaDriverEntryPointSymbolNotFound;
+  bool ok = cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &fn, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess && fn != nullptr;
+  p->write_value = reinterpret_cast<StreamWriteValue32Fn>(fn);
+  ok = ok && cudaStreamCreateWithFlags(&p->in_st, cudaStreamNonBlocking) == cudaSuccess &&
+       cudaStreamCreateWithFlags(&p->out_st, cudaStreamNonBlocking) == cudaSuccess &&
+       cudaMalloc(&p->flags, 4 * sizeof(unsigned)) == cudaSuccess &&
+       cudaMemset(p->flags, 0, 4 * sizeof(unsigned)) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
   for (int s = 0; s < 2 && ok; ++s)
-    ok = cudaEventCreateWithFlags(&p->in_done[s], cudaEventDisableTiming) == cudaSuccess &&
-         cudaEventCreateWithFlags(&p->kern_done[s], cudaEventDisableTiming) == cudaSuccess &&
+    ok = cudaEventCreateWithFlags(&p->kern_done[s], cudaEventDisableTiming) == cudaSuccess &&
          cudaEventCreateWithFlags(&p->out_done[s], cudaEventDisableTiming) == cudaSuccess &&
          cudaMalloc(&p->buf[s], bytes) == cudaSuccess;
   if (!ok) {
@@ -766,32 +790,38 @@ int dms_step_host(dms_cache_t* c, const void* k, const void* v, const float* evi
   uint8_t* b = p->buf[s];
   const size_t D = static_cast<size_t>(c->D), NH = static_cast<size_t>(c->NH);
   const size_t q_bytes = static_cast<size_t>(c->B) * q_heads * D * 2;
-  // copy in, after the kernel that last read this set
+  const unsigned seq = p->seq[s] + 1;  // this call's number on set s; the set's last copy-out wrote seq - 1
+  unsigned* flag = p->flags + 2 * s;
+  const auto write_flag = [&](unsigned* addr, cudaStream_t cs) {
+    return p->write_value(reinterpret_cast<CUstream>(cs), reinterpret_cast<CUdeviceptr>(addr), seq, 0) ==
+           CUDA_SUCCESS;
+  };
+  // copy in, after the kernel that last read this set; then flag the rows as landed
   bool ok = !p->used[s] || cudaStreamWaitEvent(p->in_st, p->kern_done[s], 0) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(b + lay.k, k, NH * D * 2, cudaMemcpyHostToDevice, p->in_st) == cudaSuccess &&
        cudaMemcpyAsync(b + lay.v, v, NH * D * 2, cudaMemcpyHostToDevice, p->in_st) == cudaSuccess &&
        cudaMemcpyAsync(b + lay.logit, evict_logit, NH * 4, cudaMemcpyHostToDevice, p->in_st) == cudaSuccess &&
        cudaMemcpyAsync(b + lay.q, q, q_bytes, cudaMemcpyHostToDevice, p->in_st) == cudaSuccess &&
-       cudaEventRecord(p->in_done[s], p->in_st) == cudaSuccess;
-  // the step, after its inputs have landed and the copy-out that last read this set's output
-  ok = ok && cudaStreamWaitEvent(st, p->in_done[s], 0) == cudaSuccess &&
-       (!p->used[s] || cudaStreamWaitEvent(st, p->out_done[s], 0) == cudaSuccess);
+       write_flag(flag, p->in_st);
   if (!ok) {
     cudaGetLastError();
-    return DMS_ERR_CUDA;
+    return DMS_ERR_CUDA;  // nothing of this call reached the compute stream; the set's numbering is unchanged
   }
-  float* o = reinterpret_cast<float*>(b + lay.out);
-  const int rc = step_launch(c, b + lay.k, b + lay.v, reinterpret_cast<const float*>(b + lay.logit), b + lay.q, o,
-                             scale, q_heads / c->H, st);
-  if (rc != DMS_OK) return rc;
-  // copy out, after the step
-  ok = cudaEventRecord(p->kern_done[s], st) == cudaSuccess &&
-       cudaStreamWaitEvent(p->out_st, p->kern_done[s], 0) == cudaSuccess &&
-       cudaMemcpyAsync(out, o, static_cast<size_t>(c->B) * q_heads * D * 4, cudaMemcpyDeviceToHost, p->out_st) ==
-           cudaSuccess &&
-       cudaEventRecord(p->out_done[s], p->out_st) == cudaSuccess;
+  p->seq[s] = seq;
   p->used[s] = true;
   p->next = s ^ 1;
+  // the step: its kernel waits (on the device) for flag[0] >= seq and flag[1] >= seq - 1
+  float* o = reinterpret_cast<float*>(b + lay.out);
+  const int rc = step_launch(c, b + lay.k, b + lay.v, reinterpret_cast<const float*>(b + lay.logit), b + lay.q, o,
+                             scale, q_heads / c->H, st, flag, seq, seq - 1);
+  // copy out after the step, then flag the output rows as read back (also when
+  // the launch failed, so that the next call on this set does not wait in vain)
+  ok = cudaEventRecord(p->kern_done[s], st) == cudaSuccess &&
+       cudaStreamWaitEvent(p->out_st, p->kern_done[s], 0) == cudaSuccess &&
+       (rc != DMS_OK || cudaMemcpyAsync(out, o, static_cast<size_t>(c->B) * q_heads * D * 4,
+                                        cudaMemcpyDeviceToHost, p->out_st) == cudaSuccess) &&
+       write_flag(flag + 1, p->out_st) && cudaEventRecord(p->out_done[s], p->out_st) == cudaSuccess;
+  if (rc != DMS_OK) return rc;
   if (!ok) {
     cudaGetLastError();
     return DMS_ERR_CUDA;

@@ -122,6 +122,13 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Load with acquire semantics at GPU scope (a flag written by another agent).
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Programmatic dependent launch: wait until the grids this one depends on have
 // completed and their writes are visible; allow the next grid in the stream to
 // be scheduled (it still waits for this grid's completion before its own wait
