@@ -210,7 +210,14 @@ int dms_step(dms_cache_t* cache, const void* k, const void* v, const float* evic
  * made (with cudaMalloc) on the first call.  Call i uses set i % 2: its
  * host->device copies wait only for the step of call i - 2, so they overlap
  * the step of call i - 1, and its device->host copy overlaps the step of
- * call i + 1.  The step itself runs on `stream`, after its own copies in.
+ * call i + 1.  The step itself runs on `stream`.  The copy streams wait for
+ * the step kernels through events; the step kernel waits for its rows (and
+ * for the copy-out of the call that last used its output rows) by polling
+ * sequence numbers that the copy streams write to device memory when they
+ * finish, so that `stream` holds only the step kernels and each step keeps
+ * the early start of dms_step.  That wait is bounded (1.5 s); on expiry the
+ * kernel latches DMS_ERR_TIMEOUT (dms_cache_status) and computes on stale
+ * rows of its own buffers.
  * Everything is asynchronous:
  *  - the host input buffers must stay unchanged, and `out` unread, until the
  *    call's copies are done: dms_step_host_join(cache, s) makes stream s wait
