@@ -725,6 +725,7 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
   if (active) is.start(lenf, i0, P0, A, E);
   cs = is;
   int n_issued = 0, n_cons = 0, nq_issued = 0, nq_conv = 0;
+  int c0_arrival = -1;  // lane 0: the count before this warp's first-segment arrival
   constexpr int QV = Sh::QV;
   uint4 qpre[QV];  // bf16 q rows of the next segment, 8 elements per chunk
 
@@ -1140,31 +1141,43 @@ __global__ void __launch_bounds__(DecodeShape<D, G, KVF>::NW * 32, 1) decode_ker
           }
           reinterpret_cast<float2*>(a.part_ml + idx * Sh::MLS)[lane] = make_float2(mm, ll);
         }
-        // The arrival is counted once the warp's range is done (below): only a
-        // warp's first and last segments can be split, and the other pieces of a
-        // head end their warps' ranges too, so the stream never waits on a count.
+        // Only a warp's first and last segments can be split.  The last one's
+        // arrival is counted once the warp's range is done (below).  The first
+        // one (ending mid-range) arrives now, its count read only at the end of
+        // the range, so the stream does not wait on it: the head's other
+        // pieces end their warps' ranges, and one of those warps merges it
+        // instead of this warp merging two heads after its range.
         if (lane == 0) {
           const int k = cs.valid ? 0 : 3;
           def[k] = seg_i;
           def[k + 1] = static_cast<int>(w0 + seg_i);
           def[k + 2] = static_cast<int>(w1 - w0) + 1;
         }
+        if (cs.valid) {
+          __syncwarp();
+          if (lane == 0) {
+            fence_release_gpu();
+            c0_arrival = atomicAdd(a.head_cnt + seg_i, 1);
+          }
+        }
       }
     }
     try_issue();
   }
-  // Count the arrivals of the warp's split segments (release the partials
-  // first); the last of a head's nseg warps merges (acquire) and resets its
-  // counter.
+  // Count the arrival of the warp's last segment if it is split (release the
+  // partial first); the last of a head's nseg warps to arrive merges
+  // (acquire) and resets its counter.
   __syncwarp();
   const int v0 = def[0], v1 = def[3];
   if (v0 >= 0 || v1 >= 0) {
     int last = 0;
     if (lane == 0) {
-      fence_release_gpu();
-      const int c0 = v0 >= 0 ? atomicAdd(a.head_cnt + v0, 1) : -1;
-      const int c1 = v1 >= 0 ? atomicAdd(a.head_cnt + v1, 1) : -1;
-      last = (v0 >= 0 && c0 == def[2] - 1 ? 1 : 0) | (v1 >= 0 && c1 == def[5] - 1 ? 2 : 0);
+      int c1 = -1;
+      if (v1 >= 0) {
+        fence_release_gpu();
+        c1 = atomicAdd(a.head_cnt + v1, 1);
+      }
+      last = (v0 >= 0 && c0_arrival == def[2] - 1 ? 1 : 0) | (v1 >= 0 && c1 == def[5] - 1 ? 2 : 0);
       if (last) fence_acquire_gpu();
     }
     last = __shfl_sync(0xffffffffu, last, 0);
