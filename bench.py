@@ -26,7 +26,6 @@ import json
 import os
 import statistics
 import sys
-import threading
 import time
 
 import torch
@@ -95,16 +94,13 @@ class _Nvml:
         if self.lib.nvmlInit_v2() != 0:
             raise RuntimeError("nvmlInit_v2 failed")
 
-    def handle(self, device_index: int):
+    def handle_from(self, pci: str, device_index: int):
+        """The NVML handle of the GPU at PCI address `pci` (as CUDA reports it),
+        else of NVML index `device_index`."""
         ct = self.ct
         h = ct.c_void_p()
-        try:
-            p = torch.cuda.get_device_properties(device_index)
-            pci = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0".encode()
-            if self.lib.nvmlDeviceGetHandleByPciBusId_v2(ct.c_char_p(pci), ct.byref(h)) == 0:
-                return h
-        except Exception:
-            pass
+        if pci and self.lib.nvmlDeviceGetHandleByPciBusId_v2(ct.c_char_p(pci.encode()), ct.byref(h)) == 0:
+            return h
         if self.lib.nvmlDeviceGetHandleByIndex_v2(ct.c_uint(device_index), ct.byref(h)) != 0:
             raise RuntimeError("no NVML handle")
         return h
@@ -125,49 +121,92 @@ class _Nvml:
         return int(v.value)
 
 
+def _clock_poll(conn, pci: str, device_index: int, period: float) -> None:
+    """Clock sampler process (spawned; no CUDA): polls the SM clock and the
+    clock-event reasons through NVML (read-only) every `period` seconds,
+    stamping each sample with time.monotonic(), until the parent sends "stop";
+    then sends the samples back."""
+    try:
+        nv = _Nvml()
+        h = nv.handle_from(pci, device_index)
+        conn.send(("ok", nv.sm_max_clock(h)))
+    except Exception as exc:
+        conn.send(("err", repr(exc)[:200]))
+        return
+    samples = []
+    while not conn.poll():
+        try:
+            samples.append((time.monotonic(), nv.sm_clock(h), nv.reasons(h)))
+        except Exception:
+            pass
+        time.sleep(period)
+    conn.recv()
+    conn.send(samples)
+
+
 class ClockSampler:
     """Polls the SM clock and clock-event reasons through NVML during the timed
-    region (read-only)."""
+    region (read-only), from a process of its own, so that the polling never
+    holds this process's interpreter lock while the timed steps are being
+    enqueued.  The sampler starts when the object is made (well before the
+    timed region) and keeps the samples stamped inside the region."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
 
-    def __init__(self, device_index: int, period_s: float = 0.0005):
+    def __init__(self, device_index: int, period_s: float = 0.0002):
+        import multiprocessing as mp
         self.period = period_s
-        self.samples, self.reasons = [], set()
-        self._stop = threading.Event()
         self.ok = False
         self.err = ""
+        self.samples, self.reasons = [], set()
+        self.t0 = self.t1 = None
         try:
-            self.nv = _Nvml()
-            self.h = self.nv.handle(device_index)
-            self.max_mhz = self.nv.sm_max_clock(self.h)
-            self.ok = True
-        except Exception as exc:  # no NVML: say so instead of clocks
-            self.err = repr(exc)[:200]
+            p = torch.cuda.get_device_properties(device_index)
+            pci = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        except Exception:
+            pci = ""
+        ctx = mp.get_context("spawn")
+        self.conn, child = ctx.Pipe()
+        self.proc = ctx.Process(target=_clock_poll, args=(child, pci, device_index, period_s), daemon=True)
+        self.proc.start()
 
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                self.samples.append(self.nv.sm_clock(self.h))
-                r = self.nv.reasons(self.h)
-                for bit, name in self.REASONS.items():
-                    if r & bit:
-                        self.reasons.add(name)
-            except Exception:
-                pass
-            time.sleep(self.period)
+    def _ready(self):
+        if self.ok or self.err:
+            return
+        try:
+            if not self.conn.poll(120):
+                raise RuntimeError("clock sampler did not start")
+            tag, val = self.conn.recv()
+        except Exception as exc:
+            tag, val = "err", repr(exc)[:200]
+        if tag == "ok":
+            self.ok, self.max_mhz = True, val
+        else:
+            self.err = val
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
-            self.t.start()
+        self._ready()
+        time.sleep(0.002)  # at least a few samples' worth of polling before the region
+        self.t0 = time.monotonic()
         return self
 
     def __exit__(self, *a):
-        self._stop.set()
+        self.t1 = time.monotonic()
         if self.ok:
-            self.t.join()
+            self.conn.send("stop")
+            allv = self.conn.recv()
+            inside = [x for x in allv if self.t0 <= x[0] <= self.t1]
+            if not inside and allv:  # a region shorter than one poll: the samples bracketing it
+                before = [x for x in allv if x[0] < self.t0][-1:]
+                after = [x for x in allv if x[0] > self.t1][:1]
+                inside = before + after
+            self.samples = [x[1] for x in inside]
+            for _, _, r in inside:
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+        self.proc.join(timeout=10)
         return False
 
     def summary(self):
@@ -175,7 +214,9 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": f"NVML unavailable: {self.err}"}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples), "source": "NVML (ctypes) polled every 0.5 ms during the timed steps"}
+                "samples": len(self.samples),
+                "source": f"NVML (ctypes) polled every {self.period * 1e3:g} ms by a separate process during the "
+                          "timed steps"}
 
 
 class _Null:
@@ -924,9 +965,9 @@ def main():
     if n0 < 1:
         ap.error("warmup + 2 * steps must be below the capacity")
 
+    clocks = ClockSampler(device.index)  # its process starts while the cache fills
     cache = fill_cache(dms, W, wl_rank, n0, device)
     ins = step_inputs(W, wl_rank, n0, args.warmup + 2 * args.steps, device)
-    clocks = ClockSampler(device.index)
     r = time_device_leg(dms, cache, ins, args.warmup, args.steps, wl.scale, device, clocks, dist)
     cache.close()
     del ins
