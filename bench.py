@@ -83,6 +83,21 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# A spin kernel of about a millisecond (torch.cuda._sleep) queued ahead of a
+# device-timed region's start event, so that all of the region's launches are
+# enqueued before the GPU reaches them: the region then times the device
+# running them back to back, not the host's launch latency and scheduling
+# jitter at its start (without it, 20-step regions on one box measured 57-74 µs
+# per step for 55 µs steps).  The end-to-end leg, which is meant to include the
+# host, is not gated.  The start event is a timing event, which ends the
+# programmatic early start, so no part of a timed step runs before it.
+GATE_CYCLES = 2_000_000
+
+
+def gate() -> None:
+    torch.cuda._sleep(GATE_CYCLES)
+
+
 class _Nvml:
     """Minimal read-only NVML access through ctypes (clock and clock-event
     reason queries only; nothing is set)."""
@@ -121,11 +136,11 @@ class _Nvml:
         return int(v.value)
 
 
-def _clock_poll(conn, pci: str, device_index: int, period: float) -> None:
-    """Clock sampler process (spawned; no CUDA): polls the SM clock and the
-    clock-event reasons through NVML (read-only) every `period` seconds,
-    stamping each sample with time.monotonic(), until the parent sends "stop";
-    then sends the samples back."""
+def _clock_poll(conn, pci: str, device_index: int) -> None:
+    """Clock sampler process (spawned; no CUDA): on each "sample" message from
+    the parent it reads the SM clock and the clock-event reasons through NVML
+    (read-only), stamped with time.monotonic(); on "stop" it sends the samples
+    back and exits."""
     try:
         nv = _Nvml()
         h = nv.handle_from(pci, device_index)
@@ -134,29 +149,31 @@ def _clock_poll(conn, pci: str, device_index: int, period: float) -> None:
         conn.send(("err", repr(exc)[:200]))
         return
     samples = []
-    while not conn.poll():
+    while True:
+        msg = conn.recv()
+        if msg == "stop":
+            conn.send(samples)
+            return
         try:
             samples.append((time.monotonic(), nv.sm_clock(h), nv.reasons(h)))
         except Exception:
             pass
-        time.sleep(period)
-    conn.recv()
-    conn.send(samples)
 
 
 class ClockSampler:
-    """Polls the SM clock and clock-event reasons through NVML during the timed
-    region (read-only), from a process of its own, so that the polling never
-    holds this process's interpreter lock while the timed steps are being
-    enqueued.  The sampler starts when the object is made (well before the
-    timed region) and keeps the samples stamped inside the region."""
+    """Reads the SM clock and clock-event reasons through NVML (read-only)
+    while the timed steps run on the GPU.  The reads are made by a process of
+    its own, on request (`sample()`, called after enqueueing some of the timed
+    steps, so that the GPU is still running them), so that they neither hold
+    this process's interpreter lock while steps are being enqueued nor poll
+    the GPU all the time (continuous NVML polling, even every 2 ms, slowed the
+    timed steps by a few per cent)."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
 
-    def __init__(self, device_index: int, period_s: float = 0.0002):
+    def __init__(self, device_index: int):
         import multiprocessing as mp
-        self.period = period_s
         self.ok = False
         self.err = ""
         self.samples, self.reasons = [], set()
@@ -168,7 +185,7 @@ class ClockSampler:
             pci = ""
         ctx = mp.get_context("spawn")
         self.conn, child = ctx.Pipe()
-        self.proc = ctx.Process(target=_clock_poll, args=(child, pci, device_index, period_s), daemon=True)
+        self.proc = ctx.Process(target=_clock_poll, args=(child, pci, device_index), daemon=True)
         self.proc.start()
 
     def _ready(self):
@@ -185,9 +202,13 @@ class ClockSampler:
         else:
             self.err = val
 
+    def sample(self):
+        """Ask for one reading now (does not wait for it)."""
+        if self.ok:
+            self.conn.send("sample")
+
     def __enter__(self):
         self._ready()
-        time.sleep(0.002)  # at least a few samples' worth of polling before the region
         self.t0 = time.monotonic()
         return self
 
@@ -195,14 +216,10 @@ class ClockSampler:
         self.t1 = time.monotonic()
         if self.ok:
             self.conn.send("stop")
-            allv = self.conn.recv()
-            inside = [x for x in allv if self.t0 <= x[0] <= self.t1]
-            if not inside and allv:  # a region shorter than one poll: the samples bracketing it
-                before = [x for x in allv if x[0] < self.t0][-1:]
-                after = [x for x in allv if x[0] > self.t1][:1]
-                inside = before + after
-            self.samples = [x[1] for x in inside]
-            for _, _, r in inside:
+            got = self.conn.recv()
+            self.samples = [x[1] for x in got]
+            self.stamps_inside = sum(1 for x in got if self.t0 <= x[0] <= self.t1)
+            for _, _, r in got:
                 for bit, name in self.REASONS.items():
                     if r & bit:
                         self.reasons.add(name)
@@ -214,9 +231,9 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": f"NVML unavailable: {self.err}"}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples),
-                "source": f"NVML (ctypes) polled every {self.period * 1e3:g} ms by a separate process during the "
-                          "timed steps"}
+                "samples": len(self.samples), "samples_inside_timed_region": self.stamps_inside,
+                "source": "NVML (ctypes), read by a separate process on request while the GPU runs the timed "
+                          "steps (after half of them and after all of them were enqueued)"}
 
 
 class _Null:
@@ -261,7 +278,8 @@ def time_device_leg(dms, cache, ins, warmup, steps, scale, device, clocks=None, 
     launch gap each.  Pass C: ``steps`` back-to-back dms_decode_attention
     calls on the final cache state, events around the whole pass -- the plain
     decode kernel's average in-stream duration.  The retained K/V (> 126 MB
-    L2) is re-read from HBM by every call."""
+    L2) is re-read from HBM by every call.  Passes A and C start behind a
+    gate() kernel, so that they time the device, not the host's launches."""
     lib = dms.load_library()
     h = cache.handle
     stream = torch.cuda.current_stream(device)
@@ -303,9 +321,12 @@ def time_device_leg(dms, cache, ins, warmup, steps, scale, device, clocks=None, 
     t_start = torch.cuda.Event(enable_timing=True)
     t_stop = torch.cuda.Event(enable_timing=True)
     with (clocks if clocks is not None else _Null()):
+        gate()
         t_start.record(stream)
         for i in range(warmup, warmup + steps):
             step(i)
+            if clocks is not None and i in (warmup + steps // 2, warmup + steps - 1):
+                clocks.sample()  # the GPU is still running the steps enqueued so far
         t_stop.record(stream)
         torch.cuda.synchronize(device)
     if dist is not None:
@@ -329,6 +350,7 @@ def time_device_leg(dms, cache, ins, warmup, steps, scale, device, clocks=None, 
     last = warmup + 2 * steps - 1
     c_start = torch.cuda.Event(enable_timing=True)
     c_stop = torch.cuda.Event(enable_timing=True)
+    gate()
     c_start.record(stream)
     for _ in range(steps):
         decode(last)
@@ -352,10 +374,10 @@ def time_e2e_leg(dms, W, wl, n0, warmup, steps, device, dist=None):
     stream, with two sets of device rows so that step i's copies overlap the
     steps i - 1 and i + 1.  The host enqueues ahead; the timed region ends
     when the last output is in host memory (host_join, then an event on the
-    compute stream).  Every step has its own output buffer; the buffers are
-    written once before the timed region, as a serving loop's reused result
-    buffers would have been (a first device write into freshly pinned pages
-    costs several times a later one).
+    compute stream).  Every step has its own input and output buffers;
+    each is copied from or to once before the timed region, as a serving
+    loop's reused buffers would have been (a first copy out of or into freshly
+    pinned pages costs several times a later one).
     Returns (ms for `steps` steps, input bytes per step, output bytes per step)."""
     cache = fill_cache(dms, W, wl, n0, device)
     ins = step_inputs(W, wl, n0, warmup + steps, device)
@@ -366,8 +388,16 @@ def time_e2e_leg(dms, W, wl, n0, warmup, steps, device, dist=None):
     out_d = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device=device)
     out_h = torch.empty((n, wl.B, wl.Hq, wl.D), dtype=torch.float32).pin_memory()
     stream = torch.cuda.current_stream(device)
+    # Every pinned buffer is read or written by a copy once before the timed
+    # region, as a serving loop's reused buffers would have been (a copy's
+    # first touch of freshly pinned pages costs several times a later one).
+    scratch = [torch.empty_like(t, device=device) for t in (qh[0], kh[0], vh[0], lh[0])]
     for i in range(n):
         out_h[i].copy_(out_d, non_blocking=True)
+        for d, hsrc in zip(scratch, (qh[i], kh[i], vh[i], lh[i])):
+            d.copy_(hsrc, non_blocking=True)
+    torch.cuda.synchronize(device)
+    del scratch
 
     def step(i):
         cache.step_host(kh[i], vh[i], lh[i], qh[i], out_h[i], wl.scale)
@@ -531,6 +561,7 @@ def time_variants(dms, W, device, steps):
         for _ in range(3):
             lib.dms_decode_attention(cache.handle, q.data_ptr(), out.data_ptr(), wl.scale, wl.Hq, stream.cuda_stream)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gate()
         e0.record(stream)
         for _ in range(steps):
             rc = lib.dms_decode_attention(cache.handle, q.data_ptr(), out.data_ptr(), wl.scale, wl.Hq,
@@ -590,6 +621,7 @@ def time_workloads(dms, W, device, steps, names=WORKLOAD_ROWS):
             step(i)
         torch.cuda.synchronize(device)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gate()
         e0.record(stream)
         for i in range(3, steps + 3):
             step(i)
@@ -605,6 +637,7 @@ def time_workloads(dms, W, device, steps, names=WORKLOAD_ROWS):
 
         for _ in range(8):
             decode()
+        gate()
         e0.record(stream)
         for _ in range(steps):
             decode()
@@ -711,6 +744,7 @@ def time_fp8_leg(dms, W, wl, device, steps):
     torch.cuda.synchronize(device)
     len0 = int(cache.lengths().sum())
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gate()
     e0.record(stream)
     for i in range(3, steps + 3):
         step(i)
@@ -718,6 +752,7 @@ def time_fp8_leg(dms, W, wl, device, steps):
     torch.cuda.synchronize(device)
     step_us = e0.elapsed_time(e1) * 1e3 / steps
     len1 = int(cache.lengths().sum())
+    gate()
     e0.record(stream)
     for _ in range(steps):
         rc = lib.dms_decode_attention(cache.handle, qs[-1].data_ptr(), out.data_ptr(), wl.scale, wl.Hq,
@@ -769,6 +804,7 @@ def time_graph_leg(dms, W, device, steps):
             fn()
         torch.cuda.synchronize(device)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gate()
         h0 = _time.perf_counter()
         e0.record(stream)
         for _ in range(steps):
@@ -1049,8 +1085,8 @@ def main():
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "note": "Python API (DmsCache.step_host = dms_step_host): each step's inputs in pinned "
                                "host memory copied in on the library's copy stream, append + decode in one launch "
-                               "on the compute stream, its output copied out to its own pinned buffer (written "
-                               "once before timing) on a second copy stream; copies of one step overlap the "
+                               "on the compute stream, its output copied out to its own pinned buffer on a "
+                               "second copy stream (every pinned buffer copied once before timing); copies of one step overlap the "
                                "neighbouring steps; timed until the last output is in host memory"}
     if not args.no_variants and world == 1:
         line["variants"] = time_variants(dms, W, device, 32)
