@@ -30,8 +30,9 @@
 //      K, V and the metadata are double-buffered: the next tile's asynchronous
 //      copies (cp.async) are in flight while this one is computed;
 //   2. one thread issues S = Q K^T (bf16 x bf16 -> fp32 in tensor memory);
-//   3. both threads of a row load the whole row of S, mask it and find its
-//      max (so they take the same decisions without talking); the running max
+//   3. each thread of a row loads its half of the row of S, masks it and
+//      finds its max, and the two threads swap their maxima through tensor
+//      memory (so they take the same decisions); the running max
 //      moves only when it grows by more than 2^8 (the accumulator in tensor
 //      memory is rescaled then); each thread turns its 64 keys into
 //      p = 2^(s - m) and keeps its half of the row sum; p is written as two bf16
@@ -67,7 +68,9 @@ struct PrefillShape {
   static constexpr int SMEM = OFF_META + 2 * NK * 8;     // 227 KB at head_dim 128
   static constexpr int TMEM_S = 0;                       // S: 2 buffers, columns [0, 2 NK)
   static constexpr int TMEM_O = 2 * NK;                  // O: columns [2 NK, 2 NK + D)
+  static constexpr int TMEM_X = 2 * NK + D;              // the two half-row maxima of each row
   static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(TMEM_X + 2 <= static_cast<int>(TMEM_COLS), "tensor memory columns");
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(G >= 1 && G <= 8, "1 <= G <= 8");
 };
@@ -293,15 +296,16 @@ __global__ void __launch_bounds__(256, 1) prefill_attention_kernel(const Prefill
     float nlg = 0.f;
     if (it + 1 < ntiles) meta_begin(it + 1, npos, nlg);
 
-    // (c) softmax of this thread's row: both threads of a row load the whole
-    // row, mask it and find its max (the same decisions without talking); each
-    // turns its own 64 keys (P panel hh) into probabilities.
-    const int2* meta = meta0 + bf * NK;
-    float s[NK];
+    // (c) softmax of this thread's row: each thread loads its own half of the
+    // row (keys hh NK/2 .. hh NK/2 + NK/2 - 1, P panel hh), masks it and finds
+    // its max; the two threads of a row (the same lane in warps w and w ^ 4)
+    // swap their maxima through tensor memory, so they take the same decisions.
+    const int2* meta = meta0 + bf * NK + hh * (NK / 2);
+    float s[NK / 2];
 #pragma unroll
-    for (int cb = 0; cb < NK / 32; ++cb) {
+    for (int cb = 0; cb < NK / 64; ++cb) {
       float v[32];
-      umma::ld32(trow + Sh::TMEM_S + bf * NK + cb * 32, v);
+      umma::ld32(trow + Sh::TMEM_S + bf * NK + hh * (NK / 2) + cb * 32, v);
 #pragma unroll
       for (int j = 0; j < 32; ++j) s[cb * 32 + j] = v[j];
     }
@@ -309,23 +313,32 @@ __global__ void __launch_bounds__(256, 1) prefill_attention_kernel(const Prefill
     if (nomask && row_ok) {
       int k0, kn;
       tile_keys(it, k0, kn);
+      kn -= hh * (NK / 2);  // this half's valid keys
 #pragma unroll
-      for (int j = 0; j < NK; j += 2) {
+      for (int j = 0; j < NK / 2; j += 2) {
         const float2 v = __fmul2_rn(make_float2(s[j], s[j + 1]), make_float2(a.qscale, a.qscale));
         s[j] = j < kn ? v.x : -INFINITY;
         s[j + 1] = j + 1 < kn ? v.y : -INFINITY;
       }
 #pragma unroll
-      for (int j = 0; j < NK; j += 4) mt = fmaxf(mt, fmaxf(fmaxf(s[j], s[j + 1]), fmaxf(s[j + 2], s[j + 3])));
+      for (int j = 0; j < NK / 2; j += 4) mt = fmaxf(mt, fmaxf(fmaxf(s[j], s[j + 1]), fmaxf(s[j + 2], s[j + 3])));
     } else {
 #pragma unroll
-      for (int j = 0; j < NK; ++j) {
+      for (int j = 0; j < NK / 2; ++j) {
         const int2 mk = meta[j];
         const bool vis = row_ok && mk.x <= tq && tq <= mk.y;
         s[j] = vis ? s[j] * a.qscale : -INFINITY;
         mt = fmaxf(mt, s[j]);
       }
     }
+    // Swap the half-row maxima: write own column, pair barrier (the two warps
+    // of this lane quarter; every thread of both reaches it once per tile),
+    // read the other's column.
+    umma::st1(trow + Sh::TMEM_X + hh, mt);
+    umma::fence_before_sync();
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
+    umma::fence_after_sync();
+    mt = fmaxf(mt, umma::ld1(trow + Sh::TMEM_X + (hh ^ 1)));
     bool rescale = false;
     float factor = 1.f;
     if (mt > m_run + 8.f) {  // also when m_run is still -inf and this tile has a visible key
@@ -343,8 +356,8 @@ __global__ void __launch_bounds__(256, 1) prefill_attention_kernel(const Prefill
     for (int qq = 0; qq < NK / 16; ++qq) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float p0 = fast_exp2((hh ? s[64 + qq * 8 + 2 * e] : s[qq * 8 + 2 * e]) - mref);
-        const float p1 = fast_exp2((hh ? s[64 + qq * 8 + 2 * e + 1] : s[qq * 8 + 2 * e + 1]) - mref);
+        const float p0 = fast_exp2(s[qq * 8 + 2 * e] - mref);
+        const float p1 = fast_exp2(s[qq * 8 + 2 * e + 1] - mref);
         psum += p0 + p1;
         const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
         const float2 hf = __bfloat1622float2(h2);

@@ -93,6 +93,25 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
 // 32 consecutive fp32 columns of this thread's lane (warp w of a warpgroup
 // reaches lanes [32 (w % 4), 32 (w % 4) + 32)).  The load and its wait are one
 // asm statement, so the compiler cannot read the registers before they land.
+// One 32-bit column of this warp's 32 lanes, each lane its own row; waits for it.
+__device__ __forceinline__ float ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r)
+      : "r"(taddr)
+      : "memory");
+  return __uint_as_float(r);
+}
+__device__ __forceinline__ void st1(uint32_t taddr, float v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v))
+      : "memory");
+}
+
 __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
