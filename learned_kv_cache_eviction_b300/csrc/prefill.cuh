@@ -350,22 +350,27 @@ __global__ void __launch_bounds__(256, 1) prefill_attention_kernel(const Prefill
       m_run = mt;
     }
     const float mref = m_run == -INFINITY ? 0.f : m_run;  // rows with nothing visible yet: p = 0
-    float psum = 0.f;
+    // Pairs of keys in packed fp32 arithmetic (each lane of a pair rounds as
+    // the scalar operation would).
+    const float2 nref = make_float2(-mref, -mref);
+    float2 psum2 = make_float2(0.f, 0.f);
     uint32_t hi[NK / 16][4], lo[NK / 16][4];
 #pragma unroll
     for (int qq = 0; qq < NK / 16; ++qq) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float p0 = fast_exp2(s[qq * 8 + 2 * e] - mref);
-        const float p1 = fast_exp2(s[qq * 8 + 2 * e + 1] - mref);
-        psum += p0 + p1;
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+        const float2 x = __fadd2_rn(make_float2(s[qq * 8 + 2 * e], s[qq * 8 + 2 * e + 1]), nref);
+        const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+        psum2 = __fadd2_rn(psum2, p);
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p.x, p.y);
         const float2 hf = __bfloat1622float2(h2);
-        const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+        const float2 d = __fadd2_rn(p, make_float2(-hf.x, -hf.y));
+        const __nv_bfloat162 l2 = __floats2bfloat162_rn(d.x, d.y);
         hi[qq][e] = *reinterpret_cast<const uint32_t*>(&h2);
         lo[qq][e] = *reinterpret_cast<const uint32_t*>(&l2);
       }
     }
+    const float psum = psum2.x + psum2.y;
 
     // (d) P V(it - 1) is done: the P buffers, O and V buffer bf ^ 1 are free.
     if (w_o < n_o) {
