@@ -279,15 +279,12 @@ __global__ void __launch_bounds__(256, 1) prefill_attention_kernel(const Prefill
     const int bf = it & 1;
     const bool nomask = nomask_next;  // every valid key of tile it is visible to every row
     // (a) S(it) is done: S buffer bf can be read, K buffer bf is free again.
-    {
-      const bool ok = mbar_wait(&bar_s, w_s & 1);
-      ++w_s;
-      if (__syncthreads_or(!ok)) {
-        failed = true;
-        break;
-      }
-      umma::fence_after_sync();
-    }
+    // Every thread observes the commit itself; a wait that timed out is only
+    // recorded here, and the CTA decides at the barrier of (g) to stop (the
+    // thread meanwhile reads stale tensor memory of its own allocation).
+    bool bad = !mbar_wait(&bar_s, w_s & 1);
+    ++w_s;
+    umma::fence_after_sync();
     // (b) prefetch K(it + 2) into K buffer bf; start loading the metadata of
     // tile it + 1 (stored in (f)).
     if (it + 2 < ntiles) stage_rows(it + 2, false);
@@ -372,14 +369,11 @@ __global__ void __launch_bounds__(256, 1) prefill_attention_kernel(const Prefill
     }
     const float psum = psum2.x + psum2.y;
 
-    // (d) P V(it - 1) is done: the P buffers, O and V buffer bf ^ 1 are free.
+    // (d) P V(it - 1) is done: the P buffers, O and V buffer bf ^ 1 are free
+    // (observed by every thread itself, as in (a)).
     if (w_o < n_o) {
-      const bool ok = mbar_wait(&bar_o, w_o & 1);
+      bad = !mbar_wait(&bar_o, w_o & 1) || bad;
       ++w_o;
-      if (__syncthreads_or(!ok)) {
-        failed = true;
-        break;
-      }
       umma::fence_after_sync();
     }
     // (e) prefetch V(it + 1) into V buffer bf ^ 1.
@@ -411,7 +405,18 @@ __global__ void __launch_bounds__(256, 1) prefill_attention_kernel(const Prefill
     umma::cp_async_wait_two();
     umma::fence_proxy_async_smem();
     umma::fence_before_sync();
-    nomask_next = __syncthreads_and(nvis);
+    // One barrier per tile in the common case: it also carries the "no mask"
+    // vote for tile it + 1 and the waits' outcome; a second one tells them
+    // apart when the vote fails (a masked next tile, or a timed-out wait).
+    if (__syncthreads_and(nvis && !bad)) {
+      nomask_next = true;
+    } else {
+      nomask_next = false;
+      if (__syncthreads_or(bad)) {
+        failed = true;
+        break;
+      }
+    }
     // (h) S(it + 1) first, so that the next softmax can start, then P V(it).
     if (tid == 0) {
       umma::fence_after_sync();
