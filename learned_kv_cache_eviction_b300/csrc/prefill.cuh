@@ -178,13 +178,18 @@ __global__ void __launch_bounds__(256, 1) prefill_attention_kernel(const Prefill
     const uint4* g = is_v ? (from_cache ? a.V : a.vc) : (from_cache ? a.K : a.kc);
     g += static_cast<size_t>(i) * (from_cache ? a.cap : a.C) * CH;
     const bool pre_swizzled = from_cache && !is_v;
-#pragma unroll 4
-    for (int x = tid; x < NK * CH; x += 256) {
-      const int j = x / CH, cc = x % CH;
-      const bool ok = j < kn;
-      const size_t src = ok ? static_cast<size_t>(k0 + j) * CH + cc : 0;
-      const int pos = pre_swizzled ? (cc & 7) : ((cc & 7) ^ (j & 7));
-      umma::cp_async16(dst + (cc >> 3) * PANEL + j * 128 + (pos << 4), g + src, ok);
+    // Thread tid copies chunk cc = tid % CH of rows j0, j0 + JS, j0 + 2 JS, ...;
+    // JS is a multiple of 8, so every one of its rows has the same swizzle.
+    constexpr int JS = 256 / CH;
+    static_assert(JS % 8 == 0 && NK % JS == 0, "rows per pass");
+    const int cc = tid % CH, j0 = tid / CH;
+    const int pos = pre_swizzled ? (cc & 7) : ((cc & 7) ^ (j0 & 7));
+    uint8_t* d0 = dst + (cc >> 3) * PANEL + j0 * 128 + (pos << 4);
+    const uint4* s0 = g + static_cast<size_t>(k0 + j0) * CH + cc;
+#pragma unroll
+    for (int k = 0; k < NK / JS; ++k) {
+      const bool ok = j0 + k * JS < kn;
+      umma::cp_async16(d0 + k * JS * 128, ok ? s0 + k * JS * CH : g, ok);
     }
   };
   // Key metadata of tile t into buffer t & 1: (position, last visible position).
@@ -310,12 +315,21 @@ __global__ void __launch_bounds__(256, 1) prefill_attention_kernel(const Prefill
     if (nomask && row_ok) {
       int k0, kn;
       tile_keys(it, k0, kn);
-      kn -= hh * (NK / 2);  // this half's valid keys
+      kn -= hh * (NK / 2);  // this half's valid keys (warp-uniform)
+      if (kn >= NK / 2) {   // a full half: no key to drop
 #pragma unroll
-      for (int j = 0; j < NK / 2; j += 2) {
-        const float2 v = __fmul2_rn(make_float2(s[j], s[j + 1]), make_float2(a.qscale, a.qscale));
-        s[j] = j < kn ? v.x : -INFINITY;
-        s[j + 1] = j + 1 < kn ? v.y : -INFINITY;
+        for (int j = 0; j < NK / 2; j += 2) {
+          const float2 v = __fmul2_rn(make_float2(s[j], s[j + 1]), make_float2(a.qscale, a.qscale));
+          s[j] = v.x;
+          s[j + 1] = v.y;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < NK / 2; j += 2) {
+          const float2 v = __fmul2_rn(make_float2(s[j], s[j + 1]), make_float2(a.qscale, a.qscale));
+          s[j] = j < kn ? v.x : -INFINITY;
+          s[j + 1] = j + 1 < kn ? v.y : -INFINITY;
+        }
       }
 #pragma unroll
       for (int j = 0; j < NK / 2; j += 4) mt = fmaxf(mt, fmaxf(fmaxf(s[j], s[j + 1]), fmaxf(s[j + 2], s[j + 3])));
