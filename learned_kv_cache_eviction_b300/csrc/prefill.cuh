@@ -303,14 +303,9 @@ __global__ void __launch_bounds__(256, 1) prefill_attention_kernel(const Prefill
     // its max; the two threads of a row (the same lane in warps w and w ^ 4)
     // swap their maxima through tensor memory, so they take the same decisions.
     const int2* meta = meta0 + bf * NK + hh * (NK / 2);
+    static_assert(NK / 2 == 64, "one 64-column load per half row");
     float s[NK / 2];
-#pragma unroll
-    for (int cb = 0; cb < NK / 64; ++cb) {
-      float v[32];
-      umma::ld32(trow + Sh::TMEM_S + bf * NK + hh * (NK / 2) + cb * 32, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) s[cb * 32 + j] = v[j];
-    }
+    umma::ld64(trow + Sh::TMEM_S + bf * NK + hh * (NK / 2), s);
     float mt = -INFINITY;
     if (nomask && row_ok) {
       int k0, kn;
