@@ -46,11 +46,44 @@ KERNEL_SOURCES = ["decode.cuh", "dms_device.cuh"]
 # helpers
 # ---------------------------------------------------------------------------
 
+def code_only(text: str) -> str:
+    """C/C++ source without its comments and blank lines, so that the stamp on
+    a profile follows the code and survives edits of comments alone."""
+    out, i, n = [], 0, len(text)
+    quote = None
+    while i < n:
+        c = text[i]
+        if quote:
+            out.append(c)
+            if c == "\\" and i + 1 < n:
+                out.append(text[i + 1])
+                i += 1
+            elif c == quote:
+                quote = None
+        elif c in "\"'":
+            quote = c
+            out.append(c)
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            continue
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            continue
+        else:
+            out.append(c)
+        i += 1
+    lines = (ln.rstrip() for ln in "".join(out).splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash() -> str:
+    """Stamp of the decode kernel's code (comments and blank lines excluded)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "learned_kv_cache_eviction_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "learned_kv_cache_eviction_b300", "csrc", f), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -66,7 +99,10 @@ def profiled_traffic():
         t = ln.strip().lstrip("-* ").strip()
         if t.startswith(("traffic_bytes_per_launch", "kernel_source_sha256")) and ":" in t:
             k, v = t.split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
+            v = v.strip()
+            if v.startswith("`"):  # the value in backticks, then an optional note
+                v = v[1:].split("`", 1)[0]
+            vals[k.strip()] = v.split()[0] if v else v
     if vals.get("kernel_source_sha256") != kernel_source_hash():
         return None
     try:

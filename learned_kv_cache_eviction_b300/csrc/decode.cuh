@@ -26,8 +26,9 @@
 //   * PV: lane owns D/32 output elements of all G heads; packed fp32 FMAs.
 // A head covered by one warp is normalised and written directly.  A head split
 // across warps leaves one partial (max, sum, unnormalised acc) per warp; each
-// such warp then increments the head's arrival counter, and the warp that
-// arrives last merges the partials and writes the output (and resets the
+// such warp then increments the head's arrival counter (a warp's first
+// segment when it ends, its last one when its range is done), and the warp
+// that arrives last merges the partials and writes the output (and resets the
 // counter for the next call).  No warp ever waits for another.
 #pragma once
 
@@ -83,10 +84,10 @@ struct DecodeShape {
   static constexpr int OFF_FX = OFF_BAR + NST * 8;
   static constexpr int FX_BYTES = (FX_T + 2) * 4;  // through the int64 position
   // Then two mbarriers for the bulk copies of a merge, and the warp's split
-  // segments whose arrivals are counted once its range is done (see
-  // decode_kernel): {virtual head, index of its first partial, partial count}
-  // for the first and for the last segment (head -1: none), and the merge
-  // mbarriers' phase bits.
+  // segments (see decode_kernel): {virtual head, index of its first partial,
+  // partial count} for the first and for the last segment (head -1: none),
+  // whose merges, if this warp's arrival completes them, run after its range;
+  // and the merge mbarriers' phase bits.
   static constexpr int OFF_MB = OFF_FX + FX_BYTES;
   static constexpr int OFF_DEF = OFF_MB + 16;
   static constexpr int WARP_BYTES = ((OFF_DEF + 28 + 127) / 128) * 128;
