@@ -113,3 +113,40 @@ def test_step_host_refuses_device_rows():
     with pytest.raises(ValueError):
         c.step_host(k, k, lg, q, out)  # the binding checks the device too
     c.close()
+
+
+def test_step_host_full_size_equals_step():
+    """The benchmark's end-to-end configuration (Qwen3-8B-like: B32, Hq32/Hkv8,
+    d128, CR 8, context 16384): 8 host-buffer steps after a 16376-token
+    history, against 8 device-row dms_step calls on a second cache with the
+    same history; outputs and bookkeeping bit-exact."""
+    wl = W.WORKLOADS["qwen3-8b"]
+    n_dec = 8
+    T0 = wl.cap - n_dec
+    a = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
+    b = dms.DmsCache(wl.B, wl.Hkv, wl.cap, wl.D, wl.w)
+    for t0 in range(0, T0, wl.chunk):
+        t1 = min(T0, t0 + wl.chunk)
+        k, v, lg = W.kv_range(wl, 0, t0, t1, device="cuda")
+        a.append_chunk(k, v, lg)
+        b.append_chunk(k, v, lg)
+        del k, v, lg
+    k, v, lg = W.kv_range(wl, 0, T0, wl.cap)
+    q = W.q_range(wl, 0, T0, wl.cap)
+    out_a = torch.empty((n_dec, wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    out_h = [torch.full((wl.B, wl.Hq, wl.D), float("nan")).pin_memory() for _ in range(n_dec)]
+    # the pinned inputs stay referenced until the copies are done
+    rows_h = [tuple(x[:, :, j].contiguous().pin_memory() for x in (k, v, lg, q)) for j in range(n_dec)]
+    for j in range(n_dec):
+        kj, vj, lj, qj = rows_h[j]
+        a.step(kj.cuda(), vj.cuda(), lj.cuda(), qj.cuda(), out_a[j], scale=wl.scale)
+        b.step_host(kj, vj, lj, qj, out_h[j], scale=wl.scale)
+    b.host_join()
+    torch.cuda.synchronize()
+    assert torch.equal(torch.stack(out_h), out_a.cpu())
+    assert torch.equal(a.lengths(), b.lengths())
+    assert torch.equal(a.slot_positions(), b.slot_positions())
+    assert a.position == b.position == wl.cap
+    assert a.status() == b.status() == dms.DMS_OK
+    a.close()
+    b.close()
