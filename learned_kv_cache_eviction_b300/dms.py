@@ -216,7 +216,8 @@ class DmsCache:
         evict_logit [B][Hkv] fp32, q [B][Hq][D] bf16 and out [B][Hq][D] fp32,
         all on the CPU (pinned memory lets the copies overlap the steps).
         Asynchronous: `out` holds the result once host_join(stream) has been
-        called and the stream synchronized."""
+        called and the stream synchronized; until then the input tensors must
+        stay alive and unchanged (the copies read them later)."""
         B, H, D = self.batch, self.kv_heads, self.head_dim
         Hq = q.shape[1] if q.dim() == 3 else -1
         cpu = torch.device("cpu")
