@@ -52,6 +52,11 @@ def _wl(B, Hq, Hkv, D, w, cap, logits, seed=31):
     (2, 4, 2, 128, 16, 200, 140, ("const", 10.0)),          # all evict: sliding window of w
     (2, 8, 4, 64, 1, 90, 70, ("normal", 0.0, 1.0)),         # eager eviction, w = 1
     (1, 8, 1, 128, 16, 40, 5, ("normal", 0.3, 2.0)),        # chunk shorter than the window
+    (2, 4, 2, 128, 16, 100, 1, ("normal", 0.5, 1.0)),       # a chunk of one token
+    (1, 12, 2, 128, 16, 256, 90, ("normal", 0.8, 1.0)),     # G 6: 21 positions per tile; cache exactly two tiles
+    (1, 14, 2, 64, 16, 70, 100, ("normal", 0.8, 1.0)),      # G 7: 18 positions per tile, padded rows
+    (1, 4, 2, 64, 64, 120, 100, ("normal", 0.5, 1.0)),      # window 64: marks pending across the whole chunk
+    (1, 4, 1, 128, 16, 0, 600, ("normal", 1.0, 1.0)),       # empty cache, 5 chunk key tiles, ragged end
 ])
 def test_prefill_matches_oracle(case):
     B, Hq, Hkv, D, w, T0, C, logits = case
