@@ -788,3 +788,38 @@ def test_qwen3_8b_decode_trajectory_1k_to_16k():
     cr = T / tr.sim.len.mean()
     assert 7.0 < cr < 9.0, cr
     tr.cache.close()
+
+
+@pytest.mark.parametrize("Hq", [4, 8])
+def test_one_head_split_over_hundreds_of_warps(Hq):
+    """One sequence with one KV head of 20000 retained slots (all keep): its
+    1250 tiles are split over ≈ 420 warps (for G = 8, each of the two query
+    groups), so one merge folds hundreds of partials in many staged chunks,
+    and the warps' first segments count their arrivals mid-range.  The plain
+    decode matches the float64 oracle; a fused step equals append + decode."""
+    wl = _small("one-head", 1, Hq, 1, 128, 16, 20004, ("const", -10.0), seed=13)
+    T = 20000
+    k, v, lg = W.kv_range(wl, 0, 0, T + 1)
+    q = W.q_range(wl, 0, T - 1, T + 1)
+    a = dms.DmsCache(1, 1, wl.cap, 128, wl.w)
+    b = dms.DmsCache(1, 1, wl.cap, 128, wl.w)
+    for c in (a, b):
+        for t0 in range(0, T, 4000):
+            c.append_chunk(k[:, :, t0:t0 + 4000].contiguous().cuda(), v[:, :, t0:t0 + 4000].contiguous().cuda(),
+                           lg[:, :, t0:t0 + 4000].contiguous().cuda())
+    out = a.decode_attention(q[:, :, 0].contiguous().cuda(), scale=wl.scale).cpu().numpy()
+    e = O.eviction_decisions(lg.numpy())
+    ref = O.decode_attention(q[:, :, 0].float().numpy(), k.float().numpy(), v.float().numpy(), e, T - 1, wl.w,
+                             wl.scale)
+    assert_attention_close(out, ref, f"one head, G {Hq}")
+    # one more token: fused step on a, append + decode on b
+    kt, vt, lt, qt = (x[:, :, -1].contiguous().cuda() for x in (k, v, lg, q))
+    out_a = torch.empty((1, Hq, 128), dtype=torch.float32, device="cuda")
+    a.step(kt, vt, lt, qt, out_a, scale=wl.scale)
+    b.append(kt, vt, lt)
+    out_b = b.decode_attention(qt, scale=wl.scale)
+    assert torch.equal(out_a, out_b)
+    assert torch.equal(a.lengths(), b.lengths())
+    assert a.status() == b.status() == dms.DMS_OK
+    a.close()
+    b.close()
